@@ -1,0 +1,206 @@
+/*
+ * hs_oracle.c -- CPU oracle for HiSparse's fused per-layer swap-in resolution.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the package smoke check and the benchmark's
+ * CPU-baseline leg may load this file's library. It shares no code, header, table or
+ * helper with the CUDA path; it is plain, single-threaded, slow-on-purpose C that a
+ * reader can check against the pages by eye.
+ *
+ * What it computes (HiSparse paper abstract; blog commentary sections two and three):
+ * every request keeps its full KV history in host memory and a small fixed-size
+ * cache of S device slots; for each layer and decode step, the k selected positions
+ * of a request are resolved by (1) hit detection through a position->slot page
+ * table, (2) LRU replacement for the misses, (3) the page-table update and (4) the
+ * host-to-device fetch of every missed entry. Only the placement of KV changes, so
+ * the rows a consumer reads through the returned slots are the host rows.
+ *
+ * The pages leave the LRU order, its tie-break and the miss/victim pairing open.
+ * This oracle takes the plainest reading that keeps the result deterministic:
+ *   - recency is a per-request call counter t (0, 1, 2, ...); a slot never used
+ *     has last_use = -1;
+ *   - slots hit in this call are stamped t and cannot be evicted in it;
+ *   - the misses, in ascending position order, take in order the non-hit slots
+ *     with the smallest (last_use, slot index);
+ *   - an evicted position is unmapped, the new one mapped and stamped t, and its
+ *     host row copied into the slot.
+ * Further readings of unstated cases:
+ *   - a negative position is padding: it resolves to -1 and is neither hit nor miss;
+ *   - a position >= C is an error: it resolves to -1, is skipped, and the call
+ *     returns a status with ORC_ERR_RANGE set;
+ *   - a position repeated within one row resolves to the same slot each time and
+ *     counts once (misses are a set of positions); the status gets ORC_ERR_DUP.
+ *
+ * Parity is pinned (not to this code itself) by: a hand-worked trace, a textbook
+ * single-access LRU cache (k = 1), an independently written recency-list LRU,
+ * closed forms for the cold start, for S >= C and for S = k, the per-step miss
+ * bound k - floor(keep * k), and the invariants of an exact cache.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_ERR_RANGE 1u
+#define ORC_ERR_DUP 2u
+#define ORC_EINVAL (-1)
+#define ORC_ENOMEM (-2)
+
+typedef struct {
+    int R, C, S, E;
+    int32_t* pt;  /* [R][C]    position -> slot, -1 when not resident */
+    int32_t* tok; /* [R][S]    slot -> position, -1 when empty        */
+    int32_t* lu;  /* [R][S]    last-use stamp, -1 when never used     */
+    int32_t* t;   /* [R]       calls made so far for the request      */
+    uint8_t* dev; /* [R][S][E] contents of the device slots           */
+} orc_state;
+
+orc_state* orc_create(int R, int C, int S, int E) {
+    if (R <= 0 || C <= 0 || S <= 0 || E <= 0) return NULL;
+    orc_state* o = (orc_state*)calloc(1, sizeof(orc_state));
+    if (!o) return NULL;
+    o->R = R; o->C = C; o->S = S; o->E = E;
+    o->pt = (int32_t*)malloc(sizeof(int32_t) * (size_t)R * C);
+    o->tok = (int32_t*)malloc(sizeof(int32_t) * (size_t)R * S);
+    o->lu = (int32_t*)malloc(sizeof(int32_t) * (size_t)R * S);
+    o->t = (int32_t*)calloc((size_t)R, sizeof(int32_t));
+    o->dev = (uint8_t*)calloc((size_t)R * S, (size_t)E);
+    if (!o->pt || !o->tok || !o->lu || !o->t || !o->dev) {
+        free(o->pt); free(o->tok); free(o->lu); free(o->t); free(o->dev); free(o);
+        return NULL;
+    }
+    for (size_t i = 0; i < (size_t)R * C; ++i) o->pt[i] = -1;
+    for (size_t i = 0; i < (size_t)R * S; ++i) { o->tok[i] = -1; o->lu[i] = -1; }
+    return o;
+}
+
+void orc_destroy(orc_state* o) {
+    if (!o) return;
+    free(o->pt); free(o->tok); free(o->lu); free(o->t); free(o->dev); free(o);
+}
+
+int32_t* orc_pt(orc_state* o) { return o->pt; }
+int32_t* orc_tok(orc_state* o) { return o->tok; }
+int32_t* orc_lu(orc_state* o) { return o->lu; }
+int32_t* orc_t(orc_state* o) { return o->t; }
+uint8_t* orc_dev(orc_state* o) { return o->dev; }
+
+/* sort helpers (the library sort is a step of the definition, nothing more) */
+static int cmp_int(const void* a, const void* b) {
+    int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+    return (x > y) - (x < y);
+}
+
+typedef struct { int32_t lu, slot; } cand_t;
+
+static int cmp_cand(const void* a, const void* b) {
+    const cand_t* x = (const cand_t*)a;
+    const cand_t* y = (const cand_t*)b;
+    if (x->lu != y->lu) return (x->lu > y->lu) - (x->lu < y->lu);
+    return (x->slot > y->slot) - (x->slot < y->slot);
+}
+
+/*
+ * Resolves one request b: host_b points at the request's history row 0 (rows are
+ * host_stride bytes apart), sel_b at its k selected positions; writes out_b[k] and
+ * *miss_b. Returns a status word (ORC_ERR_* bits) or a negative error.
+ */
+int orc_resolve_request(orc_state* o, int b, const uint8_t* host_b, size_t host_stride,
+                        const int32_t* sel_b, int k, int32_t* out_b, int32_t* miss_b) {
+    if (!o || b < 0 || b >= o->R || k <= 0 || k > o->S || !host_b || !sel_b || !out_b || !miss_b)
+        return ORC_EINVAL;
+    const int C = o->C, S = o->S, E = o->E;
+    int32_t* pt = o->pt + (size_t)b * C;
+    int32_t* tok = o->tok + (size_t)b * S;
+    int32_t* lu = o->lu + (size_t)b * S;
+    uint8_t* dev = o->dev + (size_t)b * S * E;
+    const int32_t t = o->t[b];
+    int status = 0;
+
+    char* hit = (char*)calloc((size_t)S, 1);        /* H: slots hit in this call   */
+    int32_t* P = (int32_t*)malloc(sizeof(int32_t) * (size_t)k);   /* missed positions */
+    cand_t* V = (cand_t*)malloc(sizeof(cand_t) * (size_t)S);        /* eviction order   */
+    if (!hit || !P || !V) { free(hit); free(P); free(V); return ORC_ENOMEM; }
+
+    /* 1. hit detection through the page table */
+    int np = 0;
+    for (int j = 0; j < k; ++j) {
+        int32_t p = sel_b[j];
+        out_b[j] = -1;
+        if (p < 0) continue;                         /* padding */
+        if (p >= C) { status |= ORC_ERR_RANGE; continue; }
+        if (pt[p] >= 0) {
+            out_b[j] = pt[p];
+            hit[pt[p]] = 1;
+        } else {
+            P[np++] = p;
+        }
+    }
+
+    /* 2. misses: the distinct missed positions in ascending order */
+    qsort(P, (size_t)np, sizeof(int32_t), cmp_int);
+    int m = 0;
+    for (int i = 0; i < np; ++i) {
+        if (m > 0 && P[m - 1] == P[i]) continue;
+        P[m++] = P[i];
+    }
+    /* a position repeated in the row (hit or miss) is reported */
+    {
+        int32_t* Q = (int32_t*)malloc(sizeof(int32_t) * (size_t)k);
+        if (!Q) { free(hit); free(P); free(V); return ORC_ENOMEM; }
+        int nq = 0;
+        for (int j = 0; j < k; ++j) if (sel_b[j] >= 0 && sel_b[j] < C) Q[nq++] = sel_b[j];
+        qsort(Q, (size_t)nq, sizeof(int32_t), cmp_int);
+        for (int i = 1; i < nq; ++i) if (Q[i] == Q[i - 1]) status |= ORC_ERR_DUP;
+        free(Q);
+    }
+
+    /* 3. LRU order of the slots not hit in this call: ascending (last_use, slot) */
+    int nv = 0;
+    for (int s = 0; s < S; ++s) {
+        if (hit[s]) continue;
+        V[nv].lu = lu[s];
+        V[nv].slot = s;
+        ++nv;
+    }
+    qsort(V, (size_t)nv, sizeof(cand_t), cmp_cand);
+
+    /* 4. the i-th miss takes the i-th victim: unmap, map, fetch */
+    for (int i = 0; i < m; ++i) {
+        int32_t v = V[i].slot;
+        if (tok[v] >= 0) pt[tok[v]] = -1;
+        pt[P[i]] = v;
+        tok[v] = P[i];
+        memcpy(dev + (size_t)v * E, host_b + (size_t)P[i] * host_stride, (size_t)E);
+    }
+    for (int j = 0; j < k; ++j) {
+        int32_t p = sel_b[j];
+        if (p >= 0 && p < C && out_b[j] < 0) out_b[j] = pt[p];
+    }
+
+    /* 5. stamps and counters */
+    for (int s = 0; s < S; ++s) if (hit[s]) lu[s] = t;
+    for (int i = 0; i < m; ++i) lu[V[i].slot] = t;
+    *miss_b = m;
+    o->t[b] = t + 1;
+
+    free(hit); free(P); free(V);
+    return status;
+}
+
+/*
+ * Resolves all B == R requests of one layer-step: host is [R][C] rows of
+ * host_stride bytes, sel [R][k], out [R][k], miss [R]. Returns the OR of the
+ * per-request status words, or a negative error.
+ */
+int orc_resolve(orc_state* o, const uint8_t* host, size_t host_stride, const int32_t* sel, int B,
+                int k, int32_t* out, int32_t* miss) {
+    if (!o || B != o->R || !host || !sel || !out || !miss) return ORC_EINVAL;
+    int status = 0;
+    for (int b = 0; b < B; ++b) {
+        int rc = orc_resolve_request(o, b, host + (size_t)b * o->C * host_stride, host_stride,
+                                     sel + (size_t)b * k, k, out + (size_t)b * k, miss + b);
+        if (rc < 0) return rc;
+        status |= rc;
+    }
+    return status;
+}

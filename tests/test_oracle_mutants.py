@@ -1,0 +1,55 @@
+"""Planted mistakes: each edit below breaks the oracle in a plausible way, and the
+pins of test_oracle_pins must catch every one of them.
+
+The mistakes are planted in temporary copies of the oracle's C source, compiled on
+the CPU; the oracle itself is never modified.
+"""
+import os
+
+import pytest
+
+from tests import test_oracle_pins as pins
+
+MUTANTS = {
+    "tie_break_reversed": ("return (x->slot > y->slot) - (x->slot < y->slot);",
+                           "return (x->slot < y->slot) - (x->slot > y->slot);"),
+    "misses_descending": ("return (x > y) - (x < y);", "return (x < y) - (x > y);"),
+    "hits_evictable": ("        if (hit[s]) continue;\n", ""),
+    "no_unmap": ("if (tok[v] >= 0) pt[tok[v]] = -1;", ""),
+    "hits_not_stamped": ("for (int s = 0; s < S; ++s) if (hit[s]) lu[s] = t;", ""),
+    "victims_not_stamped": ("for (int i = 0; i < m; ++i) lu[V[i].slot] = t;", ""),
+    "stamp_off_by_one": ("if (hit[s]) lu[s] = t;", "if (hit[s]) lu[s] = t + 1;"),
+    "wrong_row_fetched": ("host_b + (size_t)P[i] * host_stride", "host_b + (size_t)v * host_stride"),
+    "most_recent_victim": ("int32_t v = V[i].slot;", "int32_t v = V[nv - 1 - i].slot;"),
+    "step_not_advanced": ("o->t[b] = t + 1;", "o->t[b] = t;"),
+    "duplicate_miss_counted_twice": ("*miss_b = m;", "*miss_b = np;"),
+    "most_recent_first_order": ("if (x->lu != y->lu) return (x->lu > y->lu) - (x->lu < y->lu);",
+                                "if (x->lu != y->lu) return (x->lu < y->lu) - (x->lu > y->lu);"),
+}
+
+
+def _pin_suite(Oracle, path):
+    pins.run_hand_trace(Oracle, path)
+    pins.run_textbook_k1(Oracle, path, seeds=range(3))
+    pins.run_list_model_random(Oracle, path, seeds=range(4), steps=25)
+    pins.run_padding_range_and_duplicates(Oracle, path)
+
+
+def test_unmutated_copy_passes(oracle_mod, tmp_path):
+    src = open(oracle_mod.SRC).read()
+    p = tmp_path / "o.c"
+    p.write_text(src)
+    so = oracle_mod.compile_oracle(str(p), str(tmp_path / "o.so"))
+    _pin_suite(oracle_mod.Oracle, so)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(oracle_mod, tmp_path, name):
+    old, new = MUTANTS[name]
+    src = open(oracle_mod.SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique"
+    p = tmp_path / f"{name}.c"
+    p.write_text(src.replace(old, new))
+    so = oracle_mod.compile_oracle(str(p), str(tmp_path / f"{name}.so"))
+    with pytest.raises(AssertionError):
+        _pin_suite(oracle_mod.Oracle, so)
