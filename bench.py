@@ -1,0 +1,440 @@
+#!/usr/bin/env python3
+"""Benchmark of the HiSparse swap-in resolution step on one GB300 (or N, one rank each).
+
+A step is one hs_resolve call: every request of the DSA-style decode workload (32
+requests, one layer, context 32768, 4096 slots, k = 2048, 656-byte entries, 90 % of
+each selection kept, Zipf(1.1) refill, the 64 most recent positions always selected)
+resolved once -- hit test, LRU victims, page-table update and host->HBM fetch of the
+misses. Inputs (the selection trace, the host KV history) are resident before timing;
+L2 is flushed between timed steps.
+
+Prints one JSON line. Extra keys: miss-fetch bandwidth against the host->device peak
+measured in the same run, the no-IO (all-hit) resolution latency at 64 requests x
+k = 2048, per-kernel times, the roofline of the dominant kernel, the CPU oracle's rate
+on the host cores, and an end-to-end number through the host-buffer entry point.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from dataclasses import replace
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "top-k resolutions/s; miss-fetch GB/s vs H2D peak; µs per layer-step"
+UNIT = "resolutions/s"
+FLUSH_BYTES = 512 << 20
+H2D_PROBE_BYTES = 1 << 30
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=248)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="dsa")
+    ap.add_argument("--no-extras", action="store_true", help="skip the no-IO and CPU legs")
+    return ap.parse_args()
+
+
+def workload_for_rank(name: str, rank: int):
+    import tracegen
+    w = tracegen.WORKLOADS[name]
+    # weak scaling: every rank resolves its own requests (distinct streams per rank)
+    return w if rank == 0 else replace(w, seed=w.seed + 7919 * rank)
+
+
+def describe(w) -> str:
+    extra = f", {w.recent} most recent always selected" if w.recent else ""
+    return (f"{w.name}: {w.B} requests x {w.L} layer(s), context {w.C}, {w.S} slots, k={w.k}, "
+            f"{w.E}-byte entries, keep {w.keep_pct}%, Zipf({w.zipf_s}) refill{extra}")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.device = device
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.device)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ measurement helpers
+
+def h2d_peak_gbs(torch) -> float:
+    """Pinned host -> device cudaMemcpyAsync of 1 GiB, best of 10 (GB/s)."""
+    src = torch.empty(H2D_PROBE_BYTES, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(H2D_PROBE_BYTES, dtype=torch.uint8, device="cuda")
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = 0.0
+    for _ in range(10):
+        s.record()
+        dst.copy_(src, non_blocking=True)
+        e.record()
+        e.synchronize()
+        best = max(best, H2D_PROBE_BYTES / (s.elapsed_time(e) * 1e-3) / 1e9)
+    del src, dst
+    return best
+
+
+def resolve_hbm_bytes(w, miss) -> float:
+    """Algorithmic HBM bytes of the resolution kernel for one step (miss: per-request counts).
+
+    Per request: selections 4k, page-table probes 4k, hit stamps 4h, output 4k, and when
+    there are misses a scan of the S last-use stamps 4S, slot-token reads 4m, page-table
+    unmap + map 8m, stamps 4m, miss list 8m, plus the counters.
+    """
+    total = 0
+    for m in miss:
+        m = int(m)
+        h = w.k - m
+        b = 12 * w.k + 4 * h + 12
+        if m:
+            b += 4 * w.S + 24 * m
+        total += b
+    return float(total)
+
+
+# ------------------------------------------------------------------ reference arm (CPU oracle)
+
+def run_reference(args, rank: int, world: int) -> None:
+    if rank != 0:
+        return
+    import numpy as np
+    import tracegen
+    from oracle import Oracle
+    import oracle
+    tracegen.build()
+    oracle.build()
+    w = tracegen.WORKLOADS[args.workload]
+    T = args.warmup + args.steps
+    sel = tracegen.trace(w, T=T)
+    host = tracegen.fill_kv_array(w)
+    o = Oracle(w.B, w.C, w.S, w.E)
+    for t in range(args.warmup):
+        o.resolve(host, w.E, sel[t])
+    t0 = time.perf_counter()
+    for t in range(args.warmup, T):
+        o.resolve(host, w.E, sel[t])
+    dt = time.perf_counter() - t0
+    value = w.B * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+        "data": "synthetic",
+        "config": {"workload": describe(w), "trace_steps": f"{args.warmup} warm-up + {args.steps} timed"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"whole workload, steps {args.warmup}..{T - 1}, all {w.B} requests, "
+                                   "single-threaded C oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank: int, world: int, dist) -> None:
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    import hierarchical_kv_cache_swap_gb300 as hs
+    import tracegen
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+        __graft_entry__.build()
+
+    w = workload_for_rank(args.workload, rank)
+    K, W = args.steps, args.warmup
+    T = W + K
+    sel = tracegen.trace(w, T=T)
+    sel_dev = torch.from_numpy(sel).cuda()
+    out_dev = torch.empty_like(sel_dev)
+    miss_dev = torch.empty((T, w.B), dtype=torch.int32, device="cuda")
+    ctx = hs.Context(w.B, w.C, w.S, w.E)
+    tracegen.fill_kv(ctx.host_kv_address(), ctx.host_stride, w)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    peak_h2d = h2d_peak_gbs(torch)
+
+    def fresh():
+        ctx.reset()
+        for t in range(W):
+            ctx.resolve(sel_dev[t], out_dev[t], miss_dev[t])
+        torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    with sampler:
+        time.sleep(0.3)
+        # ---- pass 1: the step as users run it (resolution -> fetch chained by PDL)
+        fresh()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for i in range(K):
+            t = W + i
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            ctx.resolve(sel_dev[t], out_dev[t], miss_dev[t])
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        step_ms = [a.elapsed_time(b) for a, b in ev]
+        status = ctx.status()
+        miss = miss_dev[W:].cpu().numpy()
+
+        # ---- pass 2: same steps, events between the two kernels (no PDL overlap)
+        fresh()
+        pev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        for i in range(K):
+            t = W + i
+            flush.fill_(i & 0xFF)
+            ctx.resolve_profiled(sel_dev[t], out_dev[t], miss_dev[t], pev[i])
+        torch.cuda.synchronize()
+        res_ms = [e[0].elapsed_time(e[1]) for e in pev]
+        gat_ms = [e[1].elapsed_time(e[2]) for e in pev]
+
+        # ---- pass 3: end to end through the host-buffer entry point (pinned in/out)
+        fresh()
+        sel_pin = torch.from_numpy(sel).pin_memory()
+        out_pin = torch.empty((w.B, w.k), dtype=torch.int32).pin_memory()
+        miss_pin = torch.empty(w.B, dtype=torch.int32).pin_memory()
+        out_np, miss_np = out_pin.numpy(), miss_pin.numpy()
+        e2e_s = 0.0
+        for i in range(K):
+            t = W + i
+            flush.fill_(i & 0xFF)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            ctx.resolve_host(sel_pin[t].numpy(), out_np, miss_np)
+            e2e_s += time.perf_counter() - t0
+
+        # ---- no-IO: all-hit resolution at 64 requests x k = 2048 (S = 4096)
+        noio = None
+        if not args.no_extras and rank == 0:
+            noio = measure_noio(torch, hs, tracegen, flush)
+
+    clocks = sampler.summary()
+    ctx.close()
+
+    total_ms = sum(step_ms)
+    if world > 1:
+        tt = torch.tensor([total_ms, e2e_s], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms, e2e_s = float(tt[0]), float(tt[1])
+    if rank != 0:
+        return
+
+    miss_bytes = float(miss.sum()) * w.E
+    res_total, gat_total = sum(res_ms), sum(gat_ms)
+    value = world * w.B * K / (total_ms * 1e-3)
+    fetch_gbs_step = miss_bytes / (total_ms * 1e-3) / 1e9
+    fetch_gbs_kernel = miss_bytes / (gat_total * 1e-3) / 1e9 if gat_total > 0 else None
+    res_bytes = sum(resolve_hbm_bytes(w, miss[i]) for i in range(K))
+    import json as _j
+    peaks = {}
+    try:
+        peaks = _j.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except OSError:
+        pass
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    hbm_src = "MEASURED_PEAKS.json hbm_gbs" if "hbm_gbs" in peaks else "fallback 6.8 TB/s"
+    kernels = {
+        "fetch": {"ms_total": gat_total, "launches": K, "us_avg": gat_total / K * 1e3,
+                  "algorithmic_bytes_per_launch": miss_bytes / K,
+                  "achieved_gbs": fetch_gbs_kernel},
+        "resolve": {"ms_total": res_total, "launches": K, "us_avg": res_total / K * 1e3,
+                    "algorithmic_hbm_bytes_per_launch": res_bytes / K,
+                    "achieved_gbs": res_bytes / (res_total * 1e-3) / 1e9,
+                    "frac_of_hbm": res_bytes / (res_total * 1e-3) / 1e9 / hbm_peak},
+    }
+    if gat_total >= res_total:
+        roofline = {"bound": "h2d_link", "kernel": "gather_kernel", "achieved": fetch_gbs_kernel,
+                    "peak": peak_h2d, "unit": "GB/s", "frac": fetch_gbs_kernel / peak_h2d,
+                    "traffic": None,
+                    "peak_source": "pinned cudaMemcpyAsync host->device, 1 GiB, best of 10, this run"}
+    else:
+        a = res_bytes / (res_total * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": "resolve_kernel", "achieved": a, "peak": hbm_peak,
+                    "unit": "GB/s", "frac": a / hbm_peak, "traffic": None,
+                    "peak_source": hbm_src + " (of measured)"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int32", "data": "synthetic",
+        "config": {"workload": describe(w), "per_rank_requests": w.B,
+                   "trace_steps": f"{W} warm-up + {K} timed (of one seeded trace)",
+                   "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MiB write)",
+                   "timing": "CUDA events around each hs_resolve call, summed"},
+        "us_per_layer_step": total_ms / K * 1e3,
+        "positions_per_s": value * w.k,
+        "miss_fetch_gbs": fetch_gbs_step,
+        "miss_fetch_gbs_fetch_kernel": fetch_gbs_kernel,
+        "h2d_peak_gbs": peak_h2d,
+        "miss_fetch_frac_of_h2d_peak": fetch_gbs_step / peak_h2d,
+        "misses_per_step": float(miss.sum()) / K,
+        "kernels": kernels,
+        "no_io": noio,
+        "roofline": roofline,
+        "gpu_launches": K * 2,
+        "device_status": status,
+        "clocks": clocks,
+        "e2e": {"value": world * w.B * K / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": w.B * w.k * 4, "d2h_bytes_per_step": w.B * w.k * 4 + w.B * 4,
+                "how": "hs_resolve_host: pinned selections in, out_slots + miss_counts out, stream sync"},
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_extras:
+        line["cpu_baseline"] = cpu_baseline(w, ctx_host=None)
+    print(json.dumps(line), flush=True)
+
+
+def measure_noio(torch, hs, tracegen, flush) -> dict:
+    w = tracegen.noio_workload(4096)
+    N = 64
+    sel = tracegen.trace(w, T=N + 1)
+    sd = torch.from_numpy(sel).cuda()
+    out = torch.empty_like(sd)
+    miss = torch.empty((N + 1, w.B), dtype=torch.int32, device="cuda")
+    ctx = hs.Context(w.B, w.C, w.S, w.E)
+    ctx.resolve(sd[0], out[0], miss[0])  # cold call: every selection misses
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(N)]
+    for i in range(N):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record()
+        ctx.resolve(sd[i + 1], out[i + 1], miss[i + 1])
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    flushed = [a.elapsed_time(b) * 1e3 for a, b in evs]
+    assert int(miss[1:].sum()) == 0, "no-IO trace produced misses"
+    # back to back inside one CUDA graph (warm L2), as in a decode graph
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(N):
+                ctx.resolve(sd[i + 1], out[i + 1], miss[i + 1], stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    g.replay()
+    b.record()
+    b.synchronize()
+    graph_us = a.elapsed_time(b) * 1e3 / N
+    ctx.close()
+    return {"workload": describe(w) + "; every call re-selects step 0's set (all hits)",
+            "us_per_layer_step_flushed": statistics.mean(flushed),
+            "us_per_layer_step_flushed_median": statistics.median(flushed),
+            "us_per_layer_step_graph": graph_us, "calls": N}
+
+
+def cpu_baseline(w, ctx_host=None) -> dict:
+    """The CPU oracle on this host, single-threaded, on a bounded prefix of the trace."""
+    import tracegen
+    from oracle import Oracle
+    T = w.T
+    sel = tracegen.trace(w, T=T)
+    host = tracegen.fill_kv_array(w)
+    o = Oracle(w.B, w.C, w.S, w.E)
+    W = 8
+    for t in range(W):
+        o.resolve(host, w.E, sel[t])
+    t0 = time.perf_counter()
+    for t in range(W, T):
+        o.resolve(host, w.E, sel[t])
+    dt = time.perf_counter() - t0
+    return {"value": w.B * (T - W) / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{T - W} steps (after {W} untimed) x all {w.B} requests of the same workload, "
+                      "single-threaded C oracle"}
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "ours":
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

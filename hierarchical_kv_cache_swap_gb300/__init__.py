@@ -1,0 +1,222 @@
+"""GB300-native HiSparse swap-in resolution: a thin Python binding over ``libhs.so``.
+
+HiSparse (paper abstract) keeps every request's full KV history in host memory and a
+small fixed-size cache of slots on the GPU; per layer and decode step one fused
+resolution does hit detection, LRU replacement, the page-table update and the
+host-to-device fetch of the misses. All of that runs in the library's CUDA kernels
+(sm_103a) behind the C ABI of ``include/hs.h``; this module only marshals arguments
+(torch tensors or raw addresses, streams, events) to those calls. There is no
+fallback: if the compiled library is missing, loading fails with an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libhs.so")
+
+HS_OK = 0
+HS_ERR_INVALID = -1
+HS_ERR_CUDA = -2
+HS_ERR_NOMEM = -3
+HS_ERR_LIMIT = -4
+HS_STATUS_RANGE = 1
+HS_STATUS_DUP = 2
+HS_STATUS_STEP_LIMIT = 4
+HS_FLAG_NO_COPY = 1
+
+# every symbol include/hs.h declares, with (restype, argtypes)
+_VP, _I, _SZ, _U = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint
+SIGNATURES = {
+    "hs_create": (_VP, [_I, _I, _I, _I]),
+    "hs_resolve": (_I, [_VP, _VP, _VP, _I, _I, _VP, _VP]),
+    "hs_resolve_host": (_I, [_VP, _VP, _VP, _I, _I, _VP, _VP]),
+    "hs_resolve_profiled": (_I, [_VP, _VP, _VP, _I, _I, _VP, _VP, _VP]),
+    "hs_destroy": (None, [_VP]),
+    "hs_reset": (_I, [_VP, _VP]),
+    "hs_host_kv": (_VP, [_VP]),
+    "hs_host_stride": (_SZ, [_VP]),
+    "hs_device_kv": (_VP, [_VP]),
+    "hs_page_table": (_VP, [_VP]),
+    "hs_slot_token": (_VP, [_VP]),
+    "hs_last_use": (_VP, [_VP]),
+    "hs_step": (_VP, [_VP]),
+    "hs_get_status": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
+    "hs_clear_status": (_I, [_VP]),
+    "hs_set_flags": (_I, [_VP, _U]),
+    "hs_kernels_per_call": (_I, [_VP]),
+    "hs_last_error": (ctypes.c_char_p, []),
+}
+
+
+class HsError(RuntimeError):
+    pass
+
+
+_lib = None
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libhs.so in-tree with nvcc for sm_103a (see _nvcc.py)."""
+    from . import _nvcc
+    return _nvcc.build(force=force, verbose=verbose)
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libhs.so and declare its C signatures; raises if it has not been built."""
+    global _lib
+    if _lib is not None and path == LIB_PATH:
+        return _lib
+    if not os.path.exists(path):
+        raise HsError(f"{path} is missing: build it first (hierarchical_kv_cache_swap_gb300.build())")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def last_error() -> str:
+    return (load_library().hs_last_error() or b"").decode()
+
+
+def _addr(x) -> int:
+    """Device or host address of a torch tensor / numpy array / int."""
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    return x.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class _DeviceArray:
+    """Minimal __cuda_array_interface__ holder so torch can view library-owned memory."""
+
+    def __init__(self, ptr: int, shape, typestr: str, owner):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
+                                         "data": (ptr, False), "version": 3, "strides": None}
+        self._owner = owner
+
+
+class Context:
+    """One layer's cache for R requests (``hs_create``); release with close()."""
+
+    def __init__(self, num_requests: int, context_len: int, slots: int, entry_bytes: int):
+        self._lib = load_library()
+        self.R, self.C, self.S, self.E = num_requests, context_len, slots, entry_bytes
+        self._h = self._lib.hs_create(num_requests, context_len, slots, entry_bytes)
+        if not self._h:
+            raise HsError(f"hs_create failed: {last_error()}")
+        self.host_stride = int(self._lib.hs_host_stride(self._h))
+
+    # ------------------------------------------------------------------ life cycle
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            self._lib.hs_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def _check(self, rc: int, what: str) -> None:
+        if rc != HS_OK:
+            raise HsError(f"{what} failed ({rc}): {last_error()}")
+
+    # ------------------------------------------------------------------ the step
+    def resolve(self, selections, out_slots, miss_counts, stream=None) -> None:
+        """Enqueue one resolution: selections/out_slots int32 [R, k], miss_counts int32 [R] (device)."""
+        B, k = selections.shape
+        self._check(self._lib.hs_resolve(self._h, _stream(stream), _addr(selections), B, k,
+                                         _addr(out_slots), _addr(miss_counts)), "hs_resolve")
+
+    def resolve_host(self, selections: np.ndarray, out_slots: np.ndarray, miss_counts: np.ndarray,
+                     stream=None) -> None:
+        """Resolve with host buffers (copies in, resolves, copies out, waits)."""
+        B, k = selections.shape
+        self._check(self._lib.hs_resolve_host(self._h, _stream(stream), _addr(selections), B, k,
+                                              _addr(out_slots), _addr(miss_counts)),
+                    "hs_resolve_host")
+
+    def resolve_profiled(self, selections, out_slots, miss_counts, events, stream=None) -> None:
+        """resolve() that records events[0..2] around the two kernels (torch.cuda.Event)."""
+        B, k = selections.shape
+        for e in events:  # torch creates the underlying CUDA event on first record
+            if not e.cuda_event:
+                e.record(stream if stream is not None else None)
+        arr = (ctypes.c_void_p * 3)(*[e.cuda_event for e in events])
+        self._check(self._lib.hs_resolve_profiled(self._h, _stream(stream), _addr(selections), B, k,
+                                                  _addr(out_slots), _addr(miss_counts), arr),
+                    "hs_resolve_profiled")
+
+    def reset(self, stream=None) -> None:
+        self._check(self._lib.hs_reset(self._h, _stream(stream)), "hs_reset")
+
+    def set_flags(self, flags: int) -> None:
+        self._check(self._lib.hs_set_flags(self._h, flags), "hs_set_flags")
+
+    def kernels_per_call(self) -> int:
+        return int(self._lib.hs_kernels_per_call(self._h))
+
+    def status(self) -> int:
+        bits = ctypes.c_uint32(0)
+        self._check(self._lib.hs_get_status(self._h, ctypes.byref(bits)), "hs_get_status")
+        return int(bits.value)
+
+    def clear_status(self) -> None:
+        self._check(self._lib.hs_clear_status(self._h), "hs_clear_status")
+
+    # ------------------------------------------------------------------ views
+    def host_kv(self) -> np.ndarray:
+        """The pinned host store as a writable numpy view [R, C, host_stride] (uint8)."""
+        n = self.R * self.C * self.host_stride
+        buf = (ctypes.c_uint8 * n).from_address(self._lib.hs_host_kv(self._h))
+        return np.frombuffer(buf, dtype=np.uint8).reshape(self.R, self.C, self.host_stride)
+
+    def host_kv_address(self) -> int:
+        return int(self._lib.hs_host_kv(self._h))
+
+    def _dev(self, fn: str, shape, typestr: str):
+        import torch
+        return torch.as_tensor(_DeviceArray(getattr(self._lib, fn)(self._h), shape, typestr, self),
+                               device="cuda")
+
+    def device_kv(self):
+        return self._dev("hs_device_kv", (self.R, self.S, self.E), "|u1")
+
+    def page_table(self):
+        return self._dev("hs_page_table", (self.R, self.C), "<i4")
+
+    def slot_token(self):
+        return self._dev("hs_slot_token", (self.R, self.S), "<i4")
+
+    def last_use(self):
+        return self._dev("hs_last_use", (self.R, self.S), "<i4")
+
+    def step(self):
+        return self._dev("hs_step", (self.R,), "<i4")

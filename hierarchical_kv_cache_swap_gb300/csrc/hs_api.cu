@@ -1,0 +1,304 @@
+// hs_api.cu -- the C ABI of include/hs.h: allocation, argument checks, launches.
+//
+// HiSparse keeps each request's full KV history in host memory and a small fixed-size
+// cache per request on the GPU, and resolves each layer's selections inside the
+// decode CUDA graph (paper abstract). Accordingly everything is allocated once in
+// hs_create, and hs_resolve only checks its arguments on the host and enqueues the
+// two kernels: no host synchronisation, no allocation, a launch shape fixed by the
+// context, so the call can be captured in a CUDA graph and replayed.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "../../include/hs.h"
+#include "hs_internal.h"
+
+struct hs_ctx {
+    hs::Layout L;
+    int device;
+    int num_sms;
+    unsigned flags;
+    uint8_t* host_kv;      // host address of the pinned, mapped store
+    int32_t* stage_sel;    // [R][S] staging for hs_resolve_host
+    int32_t* stage_out;    // [R][S]
+    int32_t* stage_miss;   // [R]
+};
+
+namespace {
+
+thread_local char g_err[512];
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(HS_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+void free_ctx(hs_ctx* h) {
+    if (!h) return;
+    cudaFreeHost(h->host_kv);
+    cudaFree(h->L.dev);
+    cudaFree(h->L.pt);
+    cudaFree(h->L.tok);
+    cudaFree(h->L.lu);
+    cudaFree(h->L.step);
+    cudaFree(h->L.mlist);
+    cudaFree(h->L.mcnt);
+    cudaFree(h->L.status);
+    cudaFree(h->stage_sel);
+    cudaFree(h->stage_out);
+    cudaFree(h->stage_miss);
+    free(h);
+}
+
+int check_call(hs_ctx* h, const void* sel, int B, int k, const void* out, const void* miss) {
+    if (!h) return fail(HS_ERR_INVALID, "null context");
+    if (!sel || !out || !miss) return fail(HS_ERR_INVALID, "null selections/out_slots/miss_counts");
+    if (B != h->L.R) return fail(HS_ERR_INVALID, "B=%d but the context has %d requests", B, h->L.R);
+    if (k <= 0 || k > h->L.S) return fail(HS_ERR_INVALID, "k=%d must be in [1, slots=%d]", k, h->L.S);
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != h->device)
+        return fail(HS_ERR_INVALID, "current device %d is not the context's device %d", dev, h->device);
+    return HS_OK;
+}
+
+int enqueue(hs_ctx* h, cudaStream_t s, const int32_t* sel, int k, int32_t* out, int32_t* miss,
+            cudaEvent_t* ev) {
+    cudaError_t e;
+    if (ev && (e = cudaEventRecord(ev[0], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if ((e = hs::launch_resolve(h->L, s, sel, k, out, miss)) != cudaSuccess)
+        return cuda_fail(e, "resolve kernel launch");
+    if (ev && (e = cudaEventRecord(ev[1], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if (!(h->flags & HS_FLAG_NO_COPY)) {
+        if ((e = hs::launch_gather(h->L, s, h->num_sms, ev == nullptr)) != cudaSuccess)
+            return cuda_fail(e, "fetch kernel launch");
+    }
+    if (ev && (e = cudaEventRecord(ev[2], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    g_err[0] = 0;
+    return HS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* hs_last_error(void) { return g_err; }
+
+hs_ctx* hs_create(int num_requests, int context_len, int slots, int entry_bytes) {
+    const int R = num_requests, C = context_len, S = slots, E = entry_bytes;
+    if (R <= 0 || C <= 0 || S <= 0 || E <= 0) {
+        fail(HS_ERR_INVALID, "all sizes must be positive (R=%d C=%d S=%d E=%d)", R, C, S, E);
+        return nullptr;
+    }
+    if (E % 16 != 0) {
+        fail(HS_ERR_INVALID, "entry_bytes=%d must be a multiple of 16", E);
+        return nullptr;
+    }
+    if (S > hs::kMaxSlots) {
+        fail(HS_ERR_LIMIT, "slots=%d exceeds %d", S, hs::kMaxSlots);
+        return nullptr;
+    }
+    if (R > hs::kMaxRequestsGather) {
+        fail(HS_ERR_LIMIT, "num_requests=%d exceeds %d", R, hs::kMaxRequestsGather);
+        return nullptr;
+    }
+    // the fetch indexes 16-byte chunks of the miss rows with 32-bit integers
+    if ((unsigned long long)R * S * (E / 16) > (1ull << 31)) {
+        fail(HS_ERR_LIMIT, "R*S*E=%llu bytes of device buffer exceed 32 GiB",
+             (unsigned long long)R * S * E);
+        return nullptr;
+    }
+    int dev = 0, sms = 0, smem_optin = 0, can_map = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&can_map, cudaDevAttrCanMapHostMemory, dev)) != cudaSuccess) {
+        cuda_fail(e, "device query");
+        return nullptr;
+    }
+    if (!can_map) {
+        fail(HS_ERR_CUDA, "device %d cannot map host memory", dev);
+        return nullptr;
+    }
+    const size_t need = hs::resolve_smem_bytes(C, S);
+    if (need > (size_t)smem_optin || hs::gather_smem_bytes(R) > (size_t)smem_optin) {
+        fail(HS_ERR_LIMIT, "context_len=%d / slots=%d need %zu B of shared memory per CTA (max %d)", C, S,
+             need, smem_optin);
+        return nullptr;
+    }
+
+    hs_ctx* h = (hs_ctx*)calloc(1, sizeof(hs_ctx));
+    if (!h) {
+        fail(HS_ERR_NOMEM, "out of host memory");
+        return nullptr;
+    }
+    h->device = dev;
+    h->num_sms = sms;
+    hs::Layout& L = h->L;
+    L.R = R; L.C = C; L.S = S; L.E = E;
+    L.host_stride = (size_t)E;
+    const size_t host_bytes = (size_t)R * C * L.host_stride;
+    const size_t dev_bytes = (size_t)R * S * E;
+    void* hp = nullptr;
+    if ((e = cudaHostAlloc(&hp, host_bytes, cudaHostAllocMapped | cudaHostAllocPortable)) != cudaSuccess) {
+        fail(HS_ERR_NOMEM, "cudaHostAlloc of %zu bytes: %s", host_bytes, cudaGetErrorString(e));
+        free_ctx(h);
+        return nullptr;
+    }
+    h->host_kv = (uint8_t*)hp;
+    void* hdev = nullptr;
+    if ((e = cudaHostGetDevicePointer(&hdev, hp, 0)) != cudaSuccess) {
+        cuda_fail(e, "cudaHostGetDevicePointer");
+        free_ctx(h);
+        return nullptr;
+    }
+    L.host = (const uint8_t*)hdev;
+
+#define HS_ALLOC(ptr, bytes)                                                           \
+    do {                                                                              \
+        if ((e = cudaMalloc((void**)&(ptr), (bytes))) != cudaSuccess) {               \
+            fail(HS_ERR_NOMEM, "cudaMalloc of %zu bytes: %s", (size_t)(bytes),        \
+                 cudaGetErrorString(e));                                              \
+            free_ctx(h);                                                              \
+            return nullptr;                                                           \
+        }                                                                             \
+    } while (0)
+    HS_ALLOC(L.dev, dev_bytes);
+    HS_ALLOC(L.pt, sizeof(int32_t) * (size_t)R * C);
+    HS_ALLOC(L.tok, sizeof(int32_t) * (size_t)R * S);
+    HS_ALLOC(L.lu, sizeof(int32_t) * (size_t)R * S);
+    HS_ALLOC(L.step, sizeof(int32_t) * (size_t)R);
+    HS_ALLOC(L.mlist, sizeof(int2) * (size_t)R * S);
+    HS_ALLOC(L.mcnt, sizeof(int32_t) * (size_t)R);
+    HS_ALLOC(L.status, sizeof(uint32_t));
+    HS_ALLOC(h->stage_sel, sizeof(int32_t) * (size_t)R * S);
+    HS_ALLOC(h->stage_out, sizeof(int32_t) * (size_t)R * S);
+    HS_ALLOC(h->stage_miss, sizeof(int32_t) * (size_t)R);
+#undef HS_ALLOC
+
+    if ((e = hs::configure_kernels(L)) != cudaSuccess) {
+        cuda_fail(e, "kernel configuration");
+        free_ctx(h);
+        return nullptr;
+    }
+    if (hs_reset(h, nullptr) != HS_OK) {
+        free_ctx(h);
+        return nullptr;
+    }
+    if ((e = cudaStreamSynchronize(nullptr)) != cudaSuccess) {
+        cuda_fail(e, "initial reset");
+        free_ctx(h);
+        return nullptr;
+    }
+    g_err[0] = 0;
+    return h;
+}
+
+void hs_destroy(hs_ctx* h) {
+    if (!h) return;
+    cudaDeviceSynchronize();
+    free_ctx(h);
+}
+
+int hs_reset(hs_ctx* h, hs_stream_t stream) {
+    if (!h) return fail(HS_ERR_INVALID, "null context");
+    cudaStream_t s = (cudaStream_t)stream;
+    const hs::Layout& L = h->L;
+    cudaError_t e;
+    if ((e = cudaMemsetAsync(L.pt, 0xff, sizeof(int32_t) * (size_t)L.R * L.C, s)) != cudaSuccess ||
+        (e = cudaMemsetAsync(L.tok, 0xff, sizeof(int32_t) * (size_t)L.R * L.S, s)) != cudaSuccess ||
+        (e = cudaMemsetAsync(L.lu, 0xff, sizeof(int32_t) * (size_t)L.R * L.S, s)) != cudaSuccess ||
+        (e = cudaMemsetAsync(L.step, 0, sizeof(int32_t) * (size_t)L.R, s)) != cudaSuccess ||
+        (e = cudaMemsetAsync(L.mcnt, 0, sizeof(int32_t) * (size_t)L.R, s)) != cudaSuccess ||
+        (e = cudaMemsetAsync(L.status, 0, sizeof(uint32_t), s)) != cudaSuccess ||
+        (e = cudaMemsetAsync(L.dev, 0, (size_t)L.R * L.S * L.E, s)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemsetAsync");
+    return HS_OK;
+}
+
+int hs_resolve(hs_ctx* h, hs_stream_t stream, const int32_t* sel, int B, int k, int32_t* out,
+               int32_t* miss) {
+    int rc = check_call(h, sel, B, k, out, miss);
+    if (rc != HS_OK) return rc;
+    return enqueue(h, (cudaStream_t)stream, sel, k, out, miss, nullptr);
+}
+
+int hs_resolve_profiled(hs_ctx* h, hs_stream_t stream, const int32_t* sel, int B, int k, int32_t* out,
+                        int32_t* miss, hs_event_t ev[3]) {
+    int rc = check_call(h, sel, B, k, out, miss);
+    if (rc != HS_OK) return rc;
+    if (!ev || !ev[0] || !ev[1] || !ev[2]) return fail(HS_ERR_INVALID, "three events are required");
+    cudaEvent_t cev[3] = {(cudaEvent_t)ev[0], (cudaEvent_t)ev[1], (cudaEvent_t)ev[2]};
+    return enqueue(h, (cudaStream_t)stream, sel, k, out, miss, cev);
+}
+
+int hs_resolve_host(hs_ctx* h, hs_stream_t stream, const int32_t* sel_host, int B, int k,
+                    int32_t* out_host, int32_t* miss_host) {
+    int rc = check_call(h, sel_host, B, k, out_host, miss_host);
+    if (rc != HS_OK) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t n = sizeof(int32_t) * (size_t)B * k;
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(h->stage_sel, sel_host, n, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(e, "selections host->device");
+    rc = enqueue(h, s, h->stage_sel, k, h->stage_out, h->stage_miss, nullptr);
+    if (rc != HS_OK) return rc;
+    if ((e = cudaMemcpyAsync(out_host, h->stage_out, n, cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(miss_host, h->stage_miss, sizeof(int32_t) * (size_t)B, cudaMemcpyDeviceToHost,
+                             s)) != cudaSuccess)
+        return cuda_fail(e, "results device->host");
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    return HS_OK;
+}
+
+uint8_t* hs_host_kv(hs_ctx* h) { return h ? h->host_kv : nullptr; }
+size_t hs_host_stride(hs_ctx* h) { return h ? h->L.host_stride : 0; }
+uint8_t* hs_device_kv(hs_ctx* h) { return h ? h->L.dev : nullptr; }
+int32_t* hs_page_table(hs_ctx* h) { return h ? h->L.pt : nullptr; }
+int32_t* hs_slot_token(hs_ctx* h) { return h ? h->L.tok : nullptr; }
+int32_t* hs_last_use(hs_ctx* h) { return h ? h->L.lu : nullptr; }
+int32_t* hs_step(hs_ctx* h) { return h ? h->L.step : nullptr; }
+
+int hs_get_status(hs_ctx* h, uint32_t* bits) {
+    if (!h || !bits) return fail(HS_ERR_INVALID, "null argument");
+    cudaError_t e;
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    if ((e = cudaMemcpy(bits, h->L.status, sizeof(uint32_t), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e, "status read");
+    return HS_OK;
+}
+
+int hs_clear_status(hs_ctx* h) {
+    if (!h) return fail(HS_ERR_INVALID, "null context");
+    cudaError_t e;
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    if ((e = cudaMemset(h->L.status, 0, sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e, "status clear");
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    return HS_OK;
+}
+
+int hs_set_flags(hs_ctx* h, unsigned flags) {
+    if (!h) return fail(HS_ERR_INVALID, "null context");
+    if (flags & ~(unsigned)HS_FLAG_NO_COPY) return fail(HS_ERR_INVALID, "unknown flags 0x%x", flags);
+    h->flags = flags;
+    return HS_OK;
+}
+
+int hs_kernels_per_call(hs_ctx* h) {
+    if (!h) return fail(HS_ERR_INVALID, "null context");
+    return (h->flags & HS_FLAG_NO_COPY) ? 1 : 2;
+}
+
+}  // extern "C"

@@ -1,0 +1,168 @@
+/*
+ * hs.h -- C ABI of a GB300-native (sm_103a) HiSparse swap-in resolution library.
+ *
+ * HiSparse (paper abstract, "HiSparse: Turbocharging Sparse Attention with
+ * Hierarchical Memory") keeps each request's full KV history in host memory and
+ * bounds its decode footprint with a small, fixed-size GPU cache; a fused CUDA kernel
+ * resolves each layer's top-k selections -- hit detection, LRU replacement and
+ * host-to-device fetches -- inside the decode CUDA graph. The blog commentary
+ * (sections two and three) adds that the same step updates the page table and that a
+ * hit is used in place while a miss is swapped in over an LRU-chosen victim.
+ *
+ * One hs_ctx is one layer's cache for num_requests requests. It owns:
+ *   host KV store   pinned + mapped host memory, [R][C] rows of hs_host_stride() bytes
+ *                   (the first entry_bytes of each row are the entry);
+ *   device buffer   HBM, [R][S] rows of entry_bytes bytes;
+ *   page table      int32 [R][C] in HBM: position -> slot, -1 when not resident;
+ *   slot tokens     int32 [R][S]: slot -> position, -1 when empty;
+ *   last use        int32 [R][S]: per-slot recency stamp, -1 when never used;
+ *   step            int32 [R]: calls made so far per request (the stamp of the next call);
+ *   a miss list and a device status word (internal).
+ * R = num_requests, C = context_len, S = slots. Everything starts empty: page
+ * table, slot tokens and last use at -1, step 0, device buffer zero.
+ *
+ * Replacement rule (the pages leave the order open; this is the deterministic
+ * reading implemented): in a call with stamp t, slots hit by the selection are
+ * stamped t and are not evictable; the distinct missed positions, in ascending
+ * order, take in order the non-hit slots with the smallest (last_use, slot index);
+ * the position a victim held is unmapped, the new one mapped and stamped t, and its
+ * host row copied into the slot. A negative selection is padding (slot -1, neither
+ * hit nor miss); a selection >= C yields slot -1 and sets HS_STATUS_RANGE; a position
+ * repeated within one row resolves to the same slot each time, counts once, and sets
+ * HS_STATUS_DUP.
+ *
+ * Error convention: functions returning int return HS_OK (0) or a negative HS_ERR_*;
+ * hs_last_error() then describes the failure (per calling thread). Device-side input
+ * problems never trap: they set bits of the status word (hs_get_status).
+ * Threading: calls on one hs_ctx must not overlap on the GPU (state is per context);
+ * different contexts are independent.
+ */
+#ifndef HS_H_
+#define HS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct hs_ctx hs_ctx;
+/* A CUDA stream (cudaStream_t); NULL is the legacy default stream. */
+typedef struct CUstream_st* hs_stream_t;
+/* A CUDA event (cudaEvent_t). */
+typedef struct CUevent_st* hs_event_t;
+
+#define HS_OK 0
+#define HS_ERR_INVALID (-1) /* bad argument; nothing was enqueued */
+#define HS_ERR_CUDA (-2)    /* a CUDA runtime call failed */
+#define HS_ERR_NOMEM (-3)   /* host or device allocation failed */
+#define HS_ERR_LIMIT (-4)   /* sizes beyond what this build supports */
+
+/* device status bits (hs_get_status) */
+#define HS_STATUS_RANGE 1u    /* a selection was >= context_len */
+#define HS_STATUS_DUP 2u      /* a position appeared twice in one request's row */
+#define HS_STATUS_STEP_LIMIT 4u /* a request reached 2^31-1 calls; the call was skipped */
+
+/* flags (hs_set_flags) */
+#define HS_FLAG_NO_COPY 1u /* do all bookkeeping but skip the host->device row fetch */
+
+/*
+ * hs_create -- one layer's cache for num_requests requests (paper abstract: full KV
+ * history per request in host memory, a small fixed-size GPU cache per request).
+ *   num_requests  R > 0 requests
+ *   context_len   C > 0 positions of history per request (tokens, or pages)
+ *   slots         S > 0 device slots per request (the GPU cache size)
+ *   entry_bytes   E > 0 bytes per KV entry; a multiple of 16
+ * Uses the calling thread's current CUDA device. Allocates everything up front
+ * (R*C*E bytes of pinned host memory, R*S*E bytes of HBM, 4*R*(C+3S+1) bytes of
+ * tables); hs_resolve allocates nothing. Returns NULL on failure (HS_ERR_INVALID,
+ * HS_ERR_LIMIT, HS_ERR_NOMEM or HS_ERR_CUDA described by hs_last_error()). The caller
+ * owns the handle and releases it with hs_destroy.
+ */
+hs_ctx* hs_create(int num_requests, int context_len, int slots, int entry_bytes);
+
+/*
+ * hs_resolve -- the fused per-layer swap-in resolution (paper abstract: hit
+ * detection, LRU replacement and host-to-device fetches for each layer's selections;
+ * blog commentary section three: the same step updates the page table).
+ *   stream        stream to enqueue on; the call is enqueue-only (no host sync, no
+ *                 allocation), has a fixed launch shape and can be captured in a
+ *                 CUDA graph; replays advance the per-request step counters
+ *   selections    device int32 [B][k], row-major: request b's selected positions
+ *   B             must equal num_requests
+ *   k             0 < k <= slots
+ *   out_slots     device int32 [B][k]: out_slots[b][j] is the slot now holding
+ *                 selections[b][j] (-1 for padding or out-of-range); the entry's
+ *                 bytes are at hs_device_kv() + ((size_t)b * S + slot) * E
+ *   miss_counts   device int32 [B]: distinct missed positions of request b
+ * The caller owns selections/out_slots/miss_counts and keeps them alive until the
+ * enqueued work completes. Returns HS_OK, HS_ERR_INVALID (nothing enqueued) or
+ * HS_ERR_CUDA (a launch failed).
+ */
+int hs_resolve(hs_ctx* ctx, hs_stream_t stream, const int32_t* selections, int B, int k,
+               int32_t* out_slots, int32_t* miss_counts);
+
+/*
+ * hs_resolve_host -- hs_resolve with HOST buffers: copies selections host->device,
+ * resolves, copies out_slots and miss_counts device->host, and waits for the stream.
+ * Buffers may be pageable or pinned (pinned is faster). Staging buffers are
+ * preallocated by hs_create. Same arguments and errors as hs_resolve; returns after
+ * the results are in the host buffers.
+ */
+int hs_resolve_host(hs_ctx* ctx, hs_stream_t stream, const int32_t* selections_host, int B, int k,
+                    int32_t* out_slots_host, int32_t* miss_counts_host);
+
+/*
+ * hs_resolve_profiled -- hs_resolve that records ev[0] before the resolution kernel,
+ * ev[1] between it and the fetch kernel, and ev[2] after the fetch (for per-kernel
+ * timing). The two kernels are then not overlapped. ev entries must be valid events
+ * created on the context's device. Results are identical to hs_resolve.
+ */
+int hs_resolve_profiled(hs_ctx* ctx, hs_stream_t stream, const int32_t* selections, int B, int k,
+                        int32_t* out_slots, int32_t* miss_counts, hs_event_t ev[3]);
+
+/* hs_destroy -- synchronizes the device and frees everything; NULL is a no-op. */
+void hs_destroy(hs_ctx* ctx);
+
+/*
+ * hs_reset -- enqueue a reset of all state to empty on `stream` (page table, slot
+ * tokens and last use to -1, steps to 0, device buffer to zero, status cleared). The
+ * host KV store is left as it is.
+ */
+int hs_reset(hs_ctx* ctx, hs_stream_t stream);
+
+/* Host KV store: host pointer (also valid on the device through unified addressing)
+ * to [R][C] rows of hs_host_stride() bytes. The caller writes the history here before
+ * resolving; the library only reads it. */
+uint8_t* hs_host_kv(hs_ctx* ctx);
+size_t hs_host_stride(hs_ctx* ctx);
+
+/* Device pointers to the state, for consumers and tests (layouts above). The device
+ * buffer is read by the sparse-attention consumer; the tables should be treated as
+ * read-only by callers. */
+uint8_t* hs_device_kv(hs_ctx* ctx);
+int32_t* hs_page_table(hs_ctx* ctx);
+int32_t* hs_slot_token(hs_ctx* ctx);
+int32_t* hs_last_use(hs_ctx* ctx);
+int32_t* hs_step(hs_ctx* ctx);
+
+/* hs_get_status -- synchronizes the device, then stores the OR of HS_STATUS_* bits
+ * raised since the last hs_clear_status / hs_reset into *bits. */
+int hs_get_status(hs_ctx* ctx, uint32_t* bits);
+int hs_clear_status(hs_ctx* ctx);
+
+/* hs_set_flags -- HS_FLAG_* bits for later calls (0 restores the default). */
+int hs_set_flags(hs_ctx* ctx, unsigned flags);
+
+/* Number of kernels one hs_resolve call enqueues under the current flags. */
+int hs_kernels_per_call(hs_ctx* ctx);
+
+/* Description of the calling thread's last failure ("" if none). */
+const char* hs_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HS_H_ */

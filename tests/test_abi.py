@@ -1,0 +1,72 @@
+"""The C-ABI library builds, loads and exports everything include/hs.h declares.
+
+These run without a GPU: only argument checks that return before any CUDA call.
+"""
+import os
+import re
+
+import pytest
+
+import hierarchical_kv_cache_swap_gb300 as hs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hs.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    hs.build()
+    return hs.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(hs_[a-z_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("hs_create", "hs_resolve", "hs_destroy"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(names) == set(hs.SIGNATURES), "binding and header disagree"
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_library_is_built_for_sm_103a():
+    text = open(os.path.join(ROOT, "hierarchical_kv_cache_swap_gb300", "_nvcc.py")).read()
+    assert "arch=compute_103a,code=sm_103a" in text
+
+
+def test_create_rejects_bad_sizes_before_touching_cuda(lib):
+    assert not lib.hs_create(0, 8, 8, 16)
+    assert "positive" in hs.last_error()
+    assert not lib.hs_create(1, 8, 8, 24)
+    assert "multiple of 16" in hs.last_error()
+    assert not lib.hs_create(1, 8, 70000, 16)
+    assert "exceeds" in hs.last_error()
+    assert not lib.hs_create(20000, 8, 8, 16)
+    assert "exceeds" in hs.last_error()
+    assert not lib.hs_create(1 << 14, 1 << 10, 1 << 14, 1 << 12)
+    assert "32 GiB" in hs.last_error()
+
+
+def test_calls_on_null_context_fail_cleanly(lib):
+    assert lib.hs_resolve(None, None, None, 1, 1, None, None) == hs.HS_ERR_INVALID
+    assert lib.hs_resolve_host(None, None, None, 1, 1, None, None) == hs.HS_ERR_INVALID
+    assert lib.hs_set_flags(None, 0) == hs.HS_ERR_INVALID
+    assert lib.hs_reset(None, None) == hs.HS_ERR_INVALID
+    assert lib.hs_kernels_per_call(None) == hs.HS_ERR_INVALID
+    assert lib.hs_host_kv(None) is None and lib.hs_host_stride(None) == 0
+    lib.hs_destroy(None)
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    with pytest.raises(hs.HsError):
+        hs.load_library(str(tmp_path / "missing.so"))
