@@ -188,7 +188,7 @@ hs_ctx* hs_create(int num_requests, int context_len, int slots, int entry_bytes)
     HS_ALLOC(h->stage_miss, sizeof(int32_t) * (size_t)R);
 #undef HS_ALLOC
 
-    if ((e = hs::configure_kernels(L)) != cudaSuccess) {
+    if ((e = hs::configure_kernels(dev)) != cudaSuccess) {
         cuda_fail(e, "kernel configuration");
         free_ctx(h);
         return nullptr;

@@ -38,8 +38,9 @@ struct Layout {
 size_t resolve_smem_bytes(int C, int S);
 size_t gather_smem_bytes(int R);
 
-// Opt the kernels in to the shared memory they need; returns a CUDA error.
-cudaError_t configure_kernels(const Layout& L);
+// Opt the kernels in to the device's maximum dynamic shared memory (the current
+// device must be `device`); returns a CUDA error.
+cudaError_t configure_kernels(int device);
 
 // Enqueue the resolution kernel (one CTA per request).
 cudaError_t launch_resolve(const Layout& L, cudaStream_t stream, const int32_t* sel, int k,

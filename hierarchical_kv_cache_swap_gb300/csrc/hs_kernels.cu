@@ -415,12 +415,15 @@ size_t resolve_smem_bytes(int C, int S) { return SmemPlan(C, S).bytes(S); }
 
 size_t gather_smem_bytes(int R) { return (size_t)(R + 1 + kGatherThreads / 32 + 1) * 4; }
 
-cudaError_t configure_kernels(const Layout& L) {
-    cudaError_t e = cudaFuncSetAttribute(resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)resolve_smem_bytes(L.C, L.S));
+cudaError_t configure_kernels(int device) {
+    // The attribute is per kernel, not per context: opt in to the device maximum once,
+    // so that contexts of different sizes never lower each other's limit.
+    int optin = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)gather_smem_bytes(L.R));
+    e = cudaFuncSetAttribute(resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
 }
 
 cudaError_t launch_resolve(const Layout& L, cudaStream_t stream, const int32_t* sel, int k,

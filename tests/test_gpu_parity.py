@@ -262,3 +262,20 @@ def test_bad_calls_enqueue_nothing():
     torch.cuda.synchronize()
     assert (ctx.step() == 0).all()
     ctx.close()
+
+
+def test_contexts_of_different_sizes_coexist():
+    """A small context created after a large one must not break the large one's launches."""
+    big = tracegen.WORKLOADS["dsa"]
+    small = tracegen.Workload("small", 9, B=2, L=1, C=64, S=16, k=8, E=16, kv_kind=tracegen.KV_RAW,
+                              T=6, keep_pct=50, zipf_s=1.1, seed=3)
+    a = GpuRun(big, T=6, B=2)
+    b = GpuRun(small, T=6)
+    for t in range(6):
+        a.step(t)
+        b.step(t)
+    torch.cuda.synchronize()
+    a.close()
+    b.close()
+    run_and_compare(big, T=6, B=2)
+    run_and_compare(small, T=6)
