@@ -49,6 +49,8 @@ SIGNATURES = {
     "hs_set_flags": (_I, [_VP, _U]),
     "hs_kernels_per_call": (_I, [_VP]),
     "hs_last_error": (ctypes.c_char_p, []),
+    "hs_resolve_noalloc": (_I, [_VP, _I, _I, _I, _I, _VP, _SZ, _VP, _VP, _VP, _VP, _VP, _VP, _I,
+                                _VP, _VP, _VP]),
 }
 
 

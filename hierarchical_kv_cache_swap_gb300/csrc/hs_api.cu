@@ -91,6 +91,8 @@ int enqueue(hs_ctx* h, cudaStream_t s, const int32_t* sel, int k, int32_t* out, 
 
 }  // namespace
 
+void hs::record_error(const char* msg) { snprintf(g_err, sizeof g_err, "%s", msg); }
+
 extern "C" {
 
 const char* hs_last_error(void) { return g_err; }

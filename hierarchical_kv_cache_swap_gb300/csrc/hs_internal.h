@@ -50,4 +50,7 @@ cudaError_t launch_resolve(const Layout& L, cudaStream_t stream, const int32_t* 
 // dependent launch.
 cudaError_t launch_gather(const Layout& L, cudaStream_t stream, int num_sms, bool pdl);
 
+// Set the calling thread's message for hs_last_error().
+void record_error(const char* msg);
+
 }  // namespace hs

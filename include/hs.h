@@ -161,6 +161,41 @@ int hs_kernels_per_call(hs_ctx* ctx);
 /* Description of the calling thread's last failure ("" if none). */
 const char* hs_last_error(void);
 
+/*
+ * hs_resolve_noalloc -- the same resolution as hs_resolve for callers that cannot
+ * allocate device memory. The paper has no counterpart: it is a packaging of the
+ * same step. Engines that own all GPU memory through their own pool allocator, and
+ * code that sets itself up while a stream is being captured into a CUDA graph, cannot
+ * call cudaMalloc, so they cannot use hs_create. Here the caller passes every buffer,
+ * laid out as for a context (R = num_requests, C = context_len, S = slots,
+ * E = entry_bytes):
+ *   host_kv       device-visible address of the host store, [R][C] rows host_stride
+ *                 bytes apart (memory from cudaHostAlloc can be passed as is under
+ *                 unified addressing); 16-byte aligned, host_stride a multiple of 16
+ *   device_kv     [R][S][E] bytes, 16-byte aligned
+ *   page_table    int32 [R][C]; slot_token, last_use int32 [R][S]; step int32 [R]:
+ *                 the caller initialises them to -1, -1, -1 and 0 for an empty cache
+ *   selections, k, out_slots, miss_counts   as for hs_resolve (B = num_requests)
+ *   status        device uint32 that collects HS_STATUS_* bits, or NULL
+ * It allocates nothing and calls no allocating routine. The miss list the two kernels
+ * share lives in a fixed file-scope device array of HS_NOALLOC_SCRATCH_BYTES bytes,
+ * which every GPU that loads this library keeps until the process exits; calls need
+ * 8*R*S + 4*R + 4 bytes of it and larger sizes fail with HS_ERR_LIMIT before anything
+ * is enqueued. Every call on a device shares that device's copy of the array, so calls
+ * whose work overlaps on the GPU (on two streams, say) race: serialise them. The array
+ * keeps the last call's contents; every call writes what it later reads, so nothing in
+ * it needs clearing between calls. The first call on a
+ * device does a one-time set-up with that device current (it looks up the array's
+ * device address and sets kernel attributes): make that first call before any stream
+ * capture. Returns HS_OK or HS_ERR_* (hs_last_error() describes it).
+ */
+#define HS_NOALLOC_SCRATCH_BYTES (2u * 1024u * 1024u)
+int hs_resolve_noalloc(hs_stream_t stream, int num_requests, int context_len, int slots,
+                       int entry_bytes, const uint8_t* host_kv, size_t host_stride, uint8_t* device_kv,
+                       int32_t* page_table, int32_t* slot_token, int32_t* last_use, int32_t* step,
+                       const int32_t* selections, int k, int32_t* out_slots, int32_t* miss_counts,
+                       uint32_t* status);
+
 #ifdef __cplusplus
 }
 #endif

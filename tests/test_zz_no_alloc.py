@@ -1,0 +1,84 @@
+"""The allocation-free entry point gives the same results as hs_resolve.
+
+hs_resolve_noalloc exists for callers that cannot call cudaMalloc -- engines whose pool
+allocator owns all GPU memory, or set-up code running while a stream is captured into a
+CUDA graph. They pass every buffer themselves; the library's only scratch is a fixed
+device array inside the library. This test plays such a caller: it owns the state
+buffers (torch allocations standing in for the caller's pool) and checks, call after
+call, that the results are identical to the context-based entry point on the same
+inputs. Everything compared is integers or bytes, so equality is exact.
+
+The file is named to be collected last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import hierarchical_kv_cache_swap_gb300 as hs
+import tracegen
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(lib, w, host_addr, stride, st, sel, out, miss, status):
+    return lib.hs_resolve_noalloc(torch.cuda.current_stream().cuda_stream, w.B, w.C, w.S, w.E,
+                                  host_addr, stride, st["dev"].data_ptr(), st["pt"].data_ptr(),
+                                  st["tok"].data_ptr(), st["lu"].data_ptr(), st["step"].data_ptr(),
+                                  sel.data_ptr(), sel.shape[1], out.data_ptr(), miss.data_ptr(),
+                                  status.data_ptr())
+
+
+def test_noalloc_matches_resolve_call_after_call():
+    hs.build()
+    tracegen.build()
+    lib = hs.load_library()
+    w = tracegen.WORKLOADS["dsa"]  # 32 requests x 4096 slots: 1 MiB of the 2 MiB scratch
+    T = 6
+    ref = hs.Context(w.B, w.C, w.S, w.E)
+    tracegen.fill_kv(ref.host_kv_address(), ref.host_stride, w)
+    # the caller-owned state of an empty cache
+    st = {
+        "pt": torch.full((w.B, w.C), -1, dtype=torch.int32, device="cuda"),
+        "tok": torch.full((w.B, w.S), -1, dtype=torch.int32, device="cuda"),
+        "lu": torch.full((w.B, w.S), -1, dtype=torch.int32, device="cuda"),
+        "step": torch.zeros(w.B, dtype=torch.int32, device="cuda"),
+        "dev": torch.zeros((w.B, w.S, w.E), dtype=torch.uint8, device="cuda"),
+    }
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sel = torch.from_numpy(tracegen.trace(w, T=T)).cuda()
+    out_a = torch.empty_like(sel)
+    out_b = torch.empty_like(sel)
+    miss_a = torch.empty((T, w.B), dtype=torch.int32, device="cuda")
+    miss_b = torch.empty((T, w.B), dtype=torch.int32, device="cuda")
+    for t in range(T):
+        ref.resolve(sel[t], out_a[t], miss_a[t])
+        # under unified addressing the pinned host store's host pointer is device-visible
+        rc = _noalloc(lib, w, ref.host_kv_address(), ref.host_stride, st, sel[t], out_b[t],
+                      miss_b[t], status)
+        assert rc == hs.HS_OK, hs.last_error()
+        torch.cuda.synchronize()
+        assert torch.equal(out_a[t], out_b[t]), t
+        assert torch.equal(miss_a[t], miss_b[t]), t
+        assert torch.equal(ref.page_table(), st["pt"]), t
+        assert torch.equal(ref.slot_token(), st["tok"]), t
+        assert torch.equal(ref.last_use(), st["lu"]), t
+        assert torch.equal(ref.step(), st["step"]), t
+        assert torch.equal(ref.device_kv(), st["dev"]), t
+    assert int(miss_b[1:].sum()) > 0  # later calls had misses to fetch, not only the first
+    assert int(status.item()) == 0
+
+    # sizes beyond the fixed scratch array are refused before anything is enqueued
+    big = tracegen.Workload("big", 9, B=64, L=1, C=w.C, S=w.S, k=w.k, E=w.E,
+                            kv_kind=tracegen.KV_RAW, T=1, keep_pct=90, zipf_s=1.1)
+    rc = lib.hs_resolve_noalloc(None, big.B, big.C, big.S, big.E, ref.host_kv_address(),
+                                ref.host_stride, st["dev"].data_ptr(), st["pt"].data_ptr(),
+                                st["tok"].data_ptr(), st["lu"].data_ptr(), st["step"].data_ptr(),
+                                sel[0].data_ptr(), w.k, out_b[0].data_ptr(), miss_b[0].data_ptr(),
+                                None)
+    assert rc == hs.HS_ERR_LIMIT
+    assert "scratch" in hs.last_error()
+    torch.cuda.synchronize()
+    assert torch.equal(ref.step(), st["step"])
+    ref.close()
