@@ -26,6 +26,7 @@ HS_ERR_LIMIT = -4
 HS_STATUS_RANGE = 1
 HS_STATUS_DUP = 2
 HS_STATUS_STEP_LIMIT = 4
+HS_STATUS_TIMEOUT = 8
 HS_FLAG_NO_COPY = 1
 
 # every symbol include/hs.h declares, with (restype, argtypes)

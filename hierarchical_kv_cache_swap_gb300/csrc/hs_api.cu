@@ -22,6 +22,7 @@ struct hs_ctx {
     int num_sms;
     unsigned flags;
     uint8_t* host_kv;      // host address of the pinned, mapped store
+    void* miss_area;       // miss lists, counts and flags shared by the two kernels
     int32_t* stage_sel;    // [R][S] staging for hs_resolve_host
     int32_t* stage_out;    // [R][S]
     int32_t* stage_miss;   // [R]
@@ -51,8 +52,7 @@ void free_ctx(hs_ctx* h) {
     cudaFree(h->L.tok);
     cudaFree(h->L.lu);
     cudaFree(h->L.step);
-    cudaFree(h->L.mlist);
-    cudaFree(h->L.mcnt);
+    cudaFree(h->miss_area);
     cudaFree(h->L.status);
     cudaFree(h->stage_sel);
     cudaFree(h->stage_out);
@@ -75,15 +75,16 @@ int check_call(hs_ctx* h, const void* sel, int B, int k, const void* out, const 
 
 int enqueue(hs_ctx* h, cudaStream_t s, const int32_t* sel, int k, int32_t* out, int32_t* miss,
             cudaEvent_t* ev) {
+    const bool fetch = !(h->flags & HS_FLAG_NO_COPY);
     cudaError_t e;
     if (ev && (e = cudaEventRecord(ev[0], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    if ((e = hs::launch_resolve(h->L, s, sel, k, out, miss)) != cudaSuccess)
-        return cuda_fail(e, "resolve kernel launch");
+    if ((e = hs::launch_resolve(h->L, s, sel, k, out, miss, fetch)) != cudaSuccess)
+        return cuda_fail(e, "resolution kernel launch");
     if (ev && (e = cudaEventRecord(ev[1], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    if (!(h->flags & HS_FLAG_NO_COPY)) {
-        if ((e = hs::launch_gather(h->L, s, h->num_sms, ev == nullptr)) != cudaSuccess)
-            return cuda_fail(e, "fetch kernel launch");
-    }
+    // chained by programmatic dependent launch unless events sit between the kernels
+    const bool pdl = ev == nullptr && hs::overlap_fetch(h->L.R, h->num_sms);
+    if (fetch && (e = hs::launch_gather(h->L, s, h->num_sms, pdl)) != cudaSuccess)
+        return cuda_fail(e, "fetch kernel launch");
     if (ev && (e = cudaEventRecord(ev[2], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     g_err[0] = 0;
     return HS_OK;
@@ -111,8 +112,8 @@ hs_ctx* hs_create(int num_requests, int context_len, int slots, int entry_bytes)
         fail(HS_ERR_LIMIT, "slots=%d exceeds %d", S, hs::kMaxSlots);
         return nullptr;
     }
-    if (R > hs::kMaxRequestsGather) {
-        fail(HS_ERR_LIMIT, "num_requests=%d exceeds %d", R, hs::kMaxRequestsGather);
+    if (R > hs::kMaxRequests) {
+        fail(HS_ERR_LIMIT, "num_requests=%d exceeds %d", R, hs::kMaxRequests);
         return nullptr;
     }
     // the fetch indexes 16-byte chunks of the miss rows with 32-bit integers
@@ -135,7 +136,7 @@ hs_ctx* hs_create(int num_requests, int context_len, int slots, int entry_bytes)
         return nullptr;
     }
     const size_t need = hs::resolve_smem_bytes(C, S);
-    if (need > (size_t)smem_optin || hs::gather_smem_bytes(R) > (size_t)smem_optin) {
+    if (need > (size_t)smem_optin) {
         fail(HS_ERR_LIMIT, "context_len=%d / slots=%d need %zu B of shared memory per CTA (max %d)", C, S,
              need, smem_optin);
         return nullptr;
@@ -182,8 +183,8 @@ hs_ctx* hs_create(int num_requests, int context_len, int slots, int entry_bytes)
     HS_ALLOC(L.tok, sizeof(int32_t) * (size_t)R * S);
     HS_ALLOC(L.lu, sizeof(int32_t) * (size_t)R * S);
     HS_ALLOC(L.step, sizeof(int32_t) * (size_t)R);
-    HS_ALLOC(L.mlist, sizeof(int2) * (size_t)R * S);
-    HS_ALLOC(L.mcnt, sizeof(int32_t) * (size_t)R);
+    HS_ALLOC(h->miss_area, hs::miss_area_bytes(R, S));
+    hs::carve_miss_area(L, h->miss_area);
     HS_ALLOC(L.status, sizeof(uint32_t));
     HS_ALLOC(h->stage_sel, sizeof(int32_t) * (size_t)R * S);
     HS_ALLOC(h->stage_out, sizeof(int32_t) * (size_t)R * S);
@@ -223,7 +224,7 @@ int hs_reset(hs_ctx* h, hs_stream_t stream) {
         (e = cudaMemsetAsync(L.tok, 0xff, sizeof(int32_t) * (size_t)L.R * L.S, s)) != cudaSuccess ||
         (e = cudaMemsetAsync(L.lu, 0xff, sizeof(int32_t) * (size_t)L.R * L.S, s)) != cudaSuccess ||
         (e = cudaMemsetAsync(L.step, 0, sizeof(int32_t) * (size_t)L.R, s)) != cudaSuccess ||
-        (e = cudaMemsetAsync(L.mcnt, 0, sizeof(int32_t) * (size_t)L.R, s)) != cudaSuccess ||
+        (e = cudaMemsetAsync(h->miss_area, 0, hs::miss_area_bytes(L.R, L.S), s)) != cudaSuccess ||
         (e = cudaMemsetAsync(L.status, 0, sizeof(uint32_t), s)) != cudaSuccess ||
         (e = cudaMemsetAsync(L.dev, 0, (size_t)L.R * L.S * L.E, s)) != cudaSuccess)
         return cuda_fail(e, "cudaMemsetAsync");

@@ -13,11 +13,12 @@ constexpr int kRadixBits = 8;                      // LSD digit width of the vic
 constexpr int kBins = 1 << kRadixBits;
 constexpr int kGroupWords = 8;                     // bitmap words per miss-rank prefix group
 constexpr int kGatherThreads = 512;
-constexpr int kGatherCtasPerSm = 2;
+constexpr int kGatherCtasPerSm = 1;
 constexpr int kGatherUnroll = 8;                   // 16-byte loads in flight per thread
 
 constexpr int kMaxSlots = 65535;                   // slot ids are kept as uint16 in shared memory
-constexpr int kMaxRequestsGather = 16384;          // per-request miss prefix lives in shared memory
+constexpr int kMaxRequests = 1 << 20;        // requests per context
+constexpr uint32_t kSpinLimit = 1u << 21;          // bounded waits on a request's flags
 
 // Everything the two kernels need about one context.
 struct Layout {
@@ -29,25 +30,41 @@ struct Layout {
     int32_t* tok;          // [R][S]
     int32_t* lu;           // [R][S]
     int32_t* step;         // [R]
-    int2* mlist;           // [R][S]: (position, slot) of the r-th miss
-    int32_t* mcnt;         // [R]: misses of the last call
     uint32_t* status;      // device status word
+    // miss area, shared by the two kernels of a call (carve_miss_area):
+    int32_t* mpos;         // [R][S]: position of the r-th miss (ascending)
+    int32_t* mslot;        // [R][S]: slot the r-th miss takes
+    uint32_t* ready_pos;   // [R]: ((epoch_b + 1) mod 2^16) << 16 | m_b once mpos of request b is published
+    uint32_t* ready_slot;  // [R]: == epoch_b + 1 once mslot of request b is published
+    uint32_t* epoch;       // [R]: calls of request b completed by the fetch kernel
+    uint32_t* done;        // [R]: fetch CTAs of request b finished in the current call
 };
 
-// Dynamic shared memory of the resolution kernel for (C, S).
+// Bytes of the miss area for R requests of S slots, and its layout at `base`
+// (16-byte aligned). An all-zero area is a valid initial state.
+size_t miss_area_bytes(int R, int S);
+void carve_miss_area(Layout& L, void* base);
+
+// Dynamic shared memory of one request's resolution for (C, S).
 size_t resolve_smem_bytes(int C, int S);
-size_t gather_smem_bytes(int R);
+size_t gather_smem_bytes();
 
 // Opt the kernels in to the device's maximum dynamic shared memory (the current
 // device must be `device`); returns a CUDA error.
 cudaError_t configure_kernels(int device);
 
-// Enqueue the resolution kernel (one CTA per request).
+// Enqueue the resolution kernel (one CTA per request). With `fetch` (a fetch grid is
+// launched next) it publishes each request's miss positions as soon as they are
+// ranked and the victim slots once chosen.
 cudaError_t launch_resolve(const Layout& L, cudaStream_t stream, const int32_t* sel, int k,
-                           int32_t* out_slots, int32_t* miss_counts);
+                           int32_t* out_slots, int32_t* miss_counts, bool fetch);
 
-// Enqueue the row fetch; `pdl` chains it to the preceding kernel by programmatic
-// dependent launch.
+// Enqueue the row fetch (a persistent grid of kGatherCtasPerSm CTAs per SM). With
+// `pdl` it is chained to the preceding resolution by programmatic dependent launch and
+// runs concurrently with it, starting on each request's rows as soon as they are
+// published; without it, it runs after the resolution.
+// Overlap pays when the resolution leaves SMs free for the fetch grid.
+inline bool overlap_fetch(int R, int num_sms) { return R <= num_sms; }
 cudaError_t launch_gather(const Layout& L, cudaStream_t stream, int num_sms, bool pdl);
 
 // Set the calling thread's message for hs_last_error().

@@ -1,26 +1,37 @@
-// hs_kernels.cu -- the two kernels of one HiSparse swap-in resolution step, sm_103a.
+// hs_kernels.cu -- HiSparse swap-in resolution kernels for sm_103a.
 //
-// HiSparse resolves each layer's top-k selections with one fused step: hit detection,
-// LRU replacement, the page-table update and the host-to-device fetch (paper
-// abstract; blog commentary, section three). Here the step is two kernels chained by
-// programmatic dependent launch, so it stays one enqueue with no host round trip:
+// HiSparse resolves each layer's top-k selections in one fused step: hit detection,
+// LRU replacement, the page-table update and the host-to-device fetch of the misses
+// (paper abstract; blog commentary, sections two and three: hits are used in place,
+// misses swapped in over LRU victims, the page table updated in the same step).
 //
-//  resolve_kernel  one CTA per request. Probes the page table for every selected
-//                  position (hits are stamped and answered in place), marks misses
-//                  in a position bitmap (ascending-position rank = prefix popcount),
-//                  compacts the non-hit slots in slot order and ranks them by
-//                  (last_use, slot) with a stable LSD radix sort whose digits are
-//                  counted per warp (__match_any_sync ranks equal digits inside a
-//                  warp, a per-(digit, warp) exclusive scan orders the warps), pairs
-//                  the r-th miss with the r-th victim, updates page table / slot
-//                  tokens / stamps, and writes the miss list (position, slot).
-//  gather_kernel   a fixed persistent grid (2 CTAs per SM) that streams every miss
-//                  row from the mapped host store into its HBM slot with coalesced
-//                  16-byte loads, kGatherUnroll of them in flight per thread.
+// The step is two kernels that run concurrently, chained by programmatic dependent
+// launch (PDL) and synchronized per request through release/acquire flags:
 //
-// No tensor cores: nothing here is a contraction. The resolution is latency bound
-// (one dependent probe round plus shared-memory work); the fetch is bound by the
-// host link.
+// resolve_kernel -- one 512-thread CTA per request:
+//   1. probe the page table for every selected position; hits are stamped and
+//      answered in place, misses are marked in a shared position bitmap;
+//   2. rank the misses by ascending position (a group prefix over the bitmap plus
+//      popcounts), write them to the miss area and PUBLISH them (ready_pos): the
+//      source rows of the fetch are known from here on;
+//   3. rank the non-hit slots by (last_use, slot) with a stable LSD radix sort whose
+//      digits are counted per warp (__match_any_sync ranks equal digits inside a
+//      warp, an exclusive scan over the (digit, warp) table orders the warps), pair
+//      the r-th miss with the r-th victim, update page table / slot tokens / stamps,
+//      and PUBLISH the victim slots (ready_slot); answer the missed selections.
+// gather_kernel -- a persistent grid of 2 CTAs per SM, launched right behind the
+//   resolution (PDL) so that it is resident while the resolution runs. Each CTA owns
+//   a share of one request's miss rows: it waits for ready_pos, issues the 16-byte
+//   zero-copy loads of its rows from the mapped host store (coalesced, 8 in flight
+//   per thread), waits for ready_slot only when it has to store, and writes the rows
+//   into their HBM slots. The host-link transfer -- the only real cost of the step --
+//   thus overlaps the victim ranking and the table updates, and uses every SM's load
+//   slots, not just the CTAs of the requests.
+// Flags carry the value epoch_b + 1 of the call; the last fetch CTA of request b
+// advances epoch_b, so graph replays need no host reset. Every wait is bounded: on expiry
+// the CTA records HS_STATUS_TIMEOUT and skips, so no wait can hang the GPU.
+//
+// No tensor cores: nothing here is a contraction.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -29,391 +40,535 @@
 #define HS_STATUS_RANGE 1u
 #define HS_STATUS_DUP 2u
 #define HS_STATUS_STEP_LIMIT 4u
+#define HS_STATUS_TIMEOUT 8u
 
 namespace hs {
 namespace {
 
+constexpr int NT = kResolveThreads;
+constexpr int NW = kResolveWarps;
+
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait_primary() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
     return m;
 }
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
-// Exclusive scan of one value per thread over an NT-thread block. `scratch` holds
-// NT/32 + 1 words of shared memory; *total receives the block sum. Every thread
-// of the block must call it (three barriers).
-template <int NT>
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* scratch,
-                                                         uint32_t* total) {
-    constexpr int NW = NT / 32;
+// All threads' global writes so far become visible before *flag = value: the barrier
+// orders them before thread 0's release store, which is cumulative. Called by every
+// thread of the CTA; a no-op when `on` is false.
+__device__ __forceinline__ void publish(uint32_t* flag, uint32_t value, bool on) {
+    if (!on) return;
+    __syncthreads();
+    if (threadIdx.x == 0) st_release(flag, value);
+}
+
+// Thread 0 waits (bounded) until (*flag & mask) == want and broadcasts the flag's
+// value; the outcome is block-uniform. On expiry the wait records HS_STATUS_TIMEOUT
+// and returns false.
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t want, uint32_t mask,
+                                          uint32_t* status, uint32_t* bcast, uint32_t* value) {
+    if (threadIdx.x == 0) {
+        uint32_t ok = 1, it = 0, v;
+        while (((v = ld_acquire(flag)) & mask) != want) {
+            if (++it > kSpinLimit) {
+                ok = 0;
+                atomicOr(status, HS_STATUS_TIMEOUT);
+                break;
+            }
+            __nanosleep(64);
+        }
+        bcast[0] = ok;
+        bcast[1] = v;
+    }
+    __syncthreads();
+    const bool ok = bcast[0] != 0;
+    *value = bcast[1];
+    __syncthreads();
+    return ok;
+}
+
+// Exclusive scan of one value per thread over a BT-thread block. `scratch` holds
+// BT/32 + 1 words; *total receives the sum. All threads must call it (3 barriers).
+template <int BT>
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* scratch, uint32_t* total) {
+    constexpr int BW = BT / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
     if (lane == 31) scratch[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        uint32_t w = lane < NW ? scratch[lane] : 0u;
+        uint32_t w = lane < BW ? scratch[lane] : 0u;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+            const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o) w += y;
         }
-        if (lane < NW) scratch[lane] = w;
-        if (lane == NW - 1) scratch[NW] = w;
+        if (lane < BW) scratch[lane] = w;
+        if (lane == BW - 1) scratch[BW] = w;
     }
     __syncthreads();
     const uint32_t r = (warp == 0 ? 0u : scratch[warp - 1]) + x - v;
-    *total = scratch[NW];
+    *total = scratch[BW];
     __syncthreads();
     return r;
 }
 
-struct SmemPlan {
-    int CW, CG, SW, S2;
-    __host__ __device__ SmemPlan(int C, int S) {
+// Shared-memory plan of one request's resolution (byte offsets).
+struct Plan {
+    int CW, CG, SW;
+    uint32_t posbm, gprefix, hitbm, keys, mpos, counts, scratch, sa, sb, fixed;
+    __host__ __device__ Plan(int C, int S) {
         CW = ((C + 31) / 32 + kGroupWords - 1) / kGroupWords * kGroupWords;
         CG = CW / kGroupWords;
         SW = (S + 31) / 32;
-        S2 = (S + 1) & ~1;
+        const uint32_t S4 = ((uint32_t)S * 4u + 15u) & ~15u;
+        const uint32_t S2 = ((uint32_t)S * 2u + 15u) & ~15u;
+        posbm = 0;
+        gprefix = posbm + (uint32_t)CW * 4u;
+        hitbm = gprefix + (((uint32_t)CG * 4u + 15u) & ~15u);
+        keys = hitbm + (((uint32_t)SW * 4u + 15u) & ~15u);
+        mpos = keys + S4;
+        counts = mpos + S4;
+        scratch = counts + (uint32_t)(kBins * NW) * 2u;
+        sa = scratch + 48u * 4u;
+        sb = sa + S2;
+        fixed = sb + S2;
     }
-    // word offsets
-    __host__ __device__ int posbm() const { return 0; }
-    __host__ __device__ int gprefix() const { return CW; }
-    __host__ __device__ int hitbm() const { return CW + CG; }
-    __host__ __device__ int keys(int) const { return CW + CG + SW; }
-    __host__ __device__ int counts(int S) const { return keys(S) + S; }
-    __host__ __device__ int scratch(int S) const { return counts(S) + kBins * kResolveWarps; }
-    __host__ __device__ int slots(int S) const { return scratch(S) + 40; }
-    __host__ __device__ size_t bytes(int S) const {
-        return (size_t)slots(S) * 4 + (size_t)2 * S2 * sizeof(uint16_t);
+};
+
+// One request's resolution state in shared memory, and the phases shared by both
+// kernels. Every phase is called by all threads of the CTA.
+struct Request {
+    const Layout& L;
+    const Plan& P;
+    uint8_t* smem;
+    int b, k;
+    int32_t t;
+    const int32_t* selb;
+    int32_t* outb;
+    int32_t* ptb;
+    int32_t* tokb;
+    int32_t* lub;
+    uint32_t* posbm;    // missed positions of this call
+    uint32_t* gprefix;  // misses before each group of kGroupWords bitmap words
+    uint32_t* hitbm;    // slots hit in this call
+    uint32_t* keys;     // last_use + 1 of every slot
+    int32_t* mpos;      // missed positions in ascending order (rank -> position)
+    uint16_t* counts;   // radix digit counts, [digit][warp]
+    uint32_t* scratch;
+    uint16_t* sa;
+    uint16_t* sb;
+    uint32_t m = 0, N = 0, miss_base = 0, cand_base = 0;
+    int g0 = 0, g1 = 0, w0 = 0, w1 = 0;
+    const uint16_t* victims = nullptr;  // victims[r] = slot of the r-th miss
+
+    __device__ Request(const Layout& L_, const Plan& P_, uint8_t* smem_, const int32_t* sel, int k_,
+                       int32_t* out)
+        : L(L_), P(P_), smem(smem_), b(blockIdx.x), k(k_) {
+        selb = sel + (size_t)b * k;
+        outb = out + (size_t)b * k;
+        ptb = L.pt + (size_t)b * L.C;
+        tokb = L.tok + (size_t)b * L.S;
+        lub = L.lu + (size_t)b * L.S;
+        posbm = reinterpret_cast<uint32_t*>(smem + P.posbm);
+        gprefix = reinterpret_cast<uint32_t*>(smem + P.gprefix);
+        hitbm = reinterpret_cast<uint32_t*>(smem + P.hitbm);
+        keys = reinterpret_cast<uint32_t*>(smem + P.keys);
+        mpos = reinterpret_cast<int32_t*>(smem + P.mpos);
+        counts = reinterpret_cast<uint16_t*>(smem + P.counts);
+        scratch = reinterpret_cast<uint32_t*>(smem + P.scratch);
+        sa = reinterpret_cast<uint16_t*>(smem + P.sa);
+        sb = reinterpret_cast<uint16_t*>(smem + P.sb);
+    }
+
+    // Reads the step and clears the bitmaps. Returns false (after answering every
+    // selection with -1) when the request's stamps would wrap.
+    __device__ bool begin(int32_t* miss_counts) {
+        const int tid = threadIdx.x;
+        t = L.step[b];
+        for (int i = tid; i < P.CW; i += NT) posbm[i] = 0u;
+        for (int i = tid; i < P.SW; i += NT) hitbm[i] = 0u;
+        __syncthreads();
+        if (t != INT32_MAX) return true;
+        for (int j = tid; j < k; j += NT) outb[j] = -1;
+        if (tid == 0) {
+            atomicOr(L.status, HS_STATUS_STEP_LIMIT);
+            miss_counts[b] = 0;
+        }
+        return false;
+    }
+
+    // 1. hit detection. Returns true (block-uniform) if any selection missed.
+    __device__ bool probe() {
+        const int tid = threadIdx.x;
+        const int C = L.C;
+        uint32_t st = 0;
+        int any_miss = 0;
+        for (int j0 = 0; j0 < k; j0 += 4 * NT) {
+            int32_t p[4], s[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = j0 + q * NT + tid;
+                p[q] = j < k ? __ldg(selb + j) : -1;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) s[q] = (p[q] >= 0 && p[q] < C) ? ptb[p[q]] : -1;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = j0 + q * NT + tid;
+                if (j >= k) continue;
+                const int32_t pp = p[q], ss = s[q];
+                if (ss >= 0) {  // hit: answered in place, stamped, not evictable
+                    const uint32_t bit = 1u << (ss & 31);
+                    if (atomicOr(&hitbm[ss >> 5], bit) & bit) st |= HS_STATUS_DUP;
+                    lub[ss] = t;
+                    outb[j] = ss;
+                } else if (pp >= 0 && pp < C) {  // miss
+                    const uint32_t bit = 1u << (pp & 31);
+                    if (atomicOr(&posbm[pp >> 5], bit) & bit) st |= HS_STATUS_DUP;
+                    any_miss = 1;
+                } else {  // padding, or out of range
+                    if (pp >= C) st |= HS_STATUS_RANGE;
+                    outb[j] = -1;
+                }
+            }
+        }
+        if (st) atomicOr(L.status, st);
+        return __syncthreads_or(any_miss) != 0;
+    }
+
+    __device__ uint32_t word_mask(int w) const {
+        const int S = L.S;
+        return (w == P.SW - 1 && (S & 31)) ? ((1u << (S & 31)) - 1u) : 0xffffffffu;
+    }
+
+    // 2. miss count and ascending-position ranks; candidate count; mpos[] filled.
+    __device__ void rank_misses() {
+        const int tid = threadIdx.x;
+        const int S = L.S;
+        const int gpt = (P.CG + NT - 1) / NT;
+        g0 = min(tid * gpt, P.CG);
+        g1 = min(g0 + gpt, P.CG);
+        const int wpt = (P.SW + NT - 1) / NT;
+        w0 = min(tid * wpt, P.SW);
+        w1 = min(w0 + wpt, P.SW);
+        for (int s = tid; s < S; s += NT) keys[s] = (uint32_t)(lub[s] + 1);
+        uint32_t nmiss = 0, ncand = 0;
+        for (int g = g0; g < g1; ++g)
+#pragma unroll
+            for (int q = 0; q < kGroupWords; ++q) nmiss += __popc(posbm[g * kGroupWords + q]);
+        for (int w = w0; w < w1; ++w) ncand += __popc(~hitbm[w] & word_mask(w));
+        uint32_t total;
+        const uint32_t excl = block_exclusive_scan<NT>((ncand << 16) | nmiss, scratch, &total);
+        m = total & 0xffffu;
+        N = total >> 16;
+        miss_base = excl & 0xffffu;
+        cand_base = excl >> 16;
+        uint32_t r = miss_base;
+        for (int g = g0; g < g1; ++g) {
+            gprefix[g] = r;
+            for (int q = 0; q < kGroupWords; ++q) {
+                const int w = g * kGroupWords + q;
+                uint32_t bits = posbm[w];
+                while (bits) {
+                    mpos[r++] = w * 32 + __ffs(bits) - 1;
+                    bits &= bits - 1;
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // 4a. LRU order of the non-hit slots: ascending (last_use, slot); sets victims.
+    __device__ void rank_victims() {
+        const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+        uint32_t kmin = 0xffffffffu, kmax = 0u;
+        {
+            uint32_t c = cand_base;
+            for (int w = w0; w < w1; ++w) {
+                uint32_t bits = ~hitbm[w] & word_mask(w);
+                while (bits) {
+                    const int s = w * 32 + __ffs(bits) - 1;
+                    bits &= bits - 1;
+                    sa[c++] = (uint16_t)s;
+                    const uint32_t key = keys[s];
+                    kmin = min(kmin, key);
+                    kmax = max(kmax, key);
+                }
+            }
+        }
+        kmin = __reduce_min_sync(0xffffffffu, kmin);
+        kmax = __reduce_max_sync(0xffffffffu, kmax);
+        if (lane == 0) {
+            scratch[warp] = kmin;
+            scratch[NW + warp] = kmax;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            uint32_t a = scratch[0], z = scratch[NW];
+            for (int i = 1; i < NW; ++i) {
+                a = min(a, scratch[i]);
+                z = max(z, scratch[NW + i]);
+            }
+            scratch[2 * NW] = a;
+            scratch[2 * NW + 1] = z;
+        }
+        __syncthreads();
+        kmin = scratch[2 * NW];
+        kmax = scratch[2 * NW + 1];
+        __syncthreads();  // scratch is reused by the scans below
+
+        const uint32_t range = kmax - kmin;
+        const int npass = range ? (32 - __clz(range) + kRadixBits - 1) / kRadixBits : 0;
+        const int seg = (((int)N + NW - 1) / NW + 31) & ~31;
+        const int s0 = min(warp * seg, (int)N), s1 = min(s0 + seg, (int)N);
+        uint16_t* src = sa;
+        uint16_t* dst = sb;
+        for (int pass = 0; pass < npass; ++pass) {
+            const int shift = pass * kRadixBits;
+            for (int i = tid; i < kBins * NW / 2; i += NT) reinterpret_cast<uint32_t*>(counts)[i] = 0u;
+            __syncthreads();
+            for (int base = s0; base < s1; base += 32) {
+                const int idx = base + lane;
+                const bool v = idx < s1;
+                const uint32_t d = v ? ((keys[src[idx]] - kmin) >> shift) & (kBins - 1) : (uint32_t)kBins;
+                const uint32_t peers = __match_any_sync(0xffffffffu, d);
+                if (v && lane == __ffs(peers) - 1) counts[d * NW + warp] += (uint16_t)__popc(peers);
+            }
+            __syncthreads();
+            {
+                constexpr int PER = kBins * NW / NT;  // 8 counts per thread
+                uint16_t loc[PER];
+                uint32_t sum = 0;
+#pragma unroll
+                for (int q = 0; q < PER; ++q) {
+                    loc[q] = counts[tid * PER + q];
+                    sum += loc[q];
+                }
+                uint32_t tot;
+                uint32_t ex = block_exclusive_scan<NT>(sum, scratch, &tot);
+#pragma unroll
+                for (int q = 0; q < PER; ++q) {
+                    counts[tid * PER + q] = (uint16_t)ex;
+                    ex += loc[q];
+                }
+            }
+            __syncthreads();
+            for (int base = s0; base < s1; base += 32) {
+                const int idx = base + lane;
+                const bool v = idx < s1;
+                const uint16_t sl = v ? src[idx] : (uint16_t)0;
+                const uint32_t d = v ? ((keys[sl] - kmin) >> shift) & (kBins - 1) : (uint32_t)kBins;
+                const uint32_t peers = __match_any_sync(0xffffffffu, d);
+                if (v) dst[counts[d * NW + warp] + __popc(peers & lanemask_lt())] = sl;
+                __syncwarp();
+                if (v && lane == __ffs(peers) - 1) counts[d * NW + warp] += (uint16_t)__popc(peers);
+                __syncwarp();
+            }
+            __syncthreads();
+            uint16_t* tmp = src;
+            src = dst;
+            dst = tmp;
+        }
+        victims = src;
+    }
+
+    // 2b. the ranked misses into the miss area (positions, count).
+    __device__ void export_misses() {
+        int32_t* gpos = L.mpos + (size_t)b * L.S;
+        for (uint32_t r = threadIdx.x; r < m; r += NT) gpos[r] = mpos[r];
+    }
+
+    // 4b. pair, unmap, map, stamp, and export the victim slots.
+    __device__ void apply() {
+        int32_t* gslot = L.mslot + (size_t)b * L.S;
+        for (uint32_t r = threadIdx.x; r < m; r += NT) {
+            const int32_t p = mpos[r];
+            const int32_t v = victims[r];
+            const int32_t o = tokb[v];
+            if (o >= 0) ptb[o] = -1;
+            ptb[p] = v;
+            tokb[v] = p;
+            lub[v] = t;
+            gslot[r] = v;
+        }
+    }
+
+    // 4c. answers for the missed selections (their rank through the bitmap).
+    __device__ void answer_misses() {
+        const int C = L.C;
+        for (int j = threadIdx.x; j < k; j += NT) {
+            const int32_t p = __ldg(selb + j);
+            if (p < 0 || p >= C) continue;
+            const int w = p >> 5;
+            const uint32_t bit = 1u << (p & 31);
+            const uint32_t word = posbm[w];
+            if (!(word & bit)) continue;  // a hit, already answered
+            const int g = w / kGroupWords;
+            uint32_t rank = gprefix[g];
+            for (int q = g * kGroupWords; q < w; ++q) rank += __popc(posbm[q]);
+            rank += __popc(word & (bit - 1u));
+            outb[j] = victims[rank];
+        }
+    }
+
+    __device__ void finish(int32_t* miss_counts, uint32_t misses) {
+        if (threadIdx.x == 0) {
+            miss_counts[b] = (int32_t)misses;
+            L.step[b] = t + 1;
+        }
     }
 };
 
 __global__ void __launch_bounds__(kResolveThreads, 2)
 resolve_kernel(const Layout L, const int32_t* __restrict__ sel, int k, int32_t* __restrict__ out,
-               int32_t* __restrict__ miss_counts) {
-    constexpr int NT = kResolveThreads;
-    extern __shared__ __align__(16) uint32_t smem[];
-    const int C = L.C, S = L.S;
-    const SmemPlan P(C, S);
-    uint32_t* posbm = smem + P.posbm();     // missed positions of this call
-    uint32_t* gprefix = smem + P.gprefix(); // misses before each group of kGroupWords words
-    uint32_t* hitbm = smem + P.hitbm();     // slots hit in this call
-    uint32_t* keys = smem + P.keys(S);      // last_use + 1 per slot; later miss positions by rank
-    uint32_t* counts = smem + P.counts(S);  // radix digit counts, [digit][warp]
-    uint32_t* scratch = smem + P.scratch(S);
-    uint16_t* sa = reinterpret_cast<uint16_t*>(smem + P.slots(S));
-    uint16_t* sb = sa + P.S2;
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int b = blockIdx.x;
-    const int32_t* selb = sel + (size_t)b * k;
-    int32_t* outb = out + (size_t)b * k;
-    int32_t* ptb = L.pt + (size_t)b * C;
-    int32_t* tokb = L.tok + (size_t)b * S;
-    int32_t* lub = L.lu + (size_t)b * S;
-
-    // The fetch kernel may be scheduled now; it waits for this grid to finish.
-    pdl_launch_dependents();
-
-    const int32_t t = L.step[b];
-    for (int i = tid; i < P.CW; i += NT) posbm[i] = 0u;
-    for (int i = tid; i < P.SW; i += NT) hitbm[i] = 0u;
-    __syncthreads();
-
-    if (t == INT32_MAX) {  // stamps would wrap: refuse the call for this request
-        for (int j = tid; j < k; j += NT) outb[j] = -1;
-        if (tid == 0) {
-            atomicOr(L.status, HS_STATUS_STEP_LIMIT);
-            miss_counts[b] = 0;
-            L.mcnt[b] = 0;
-        }
+               int32_t* __restrict__ miss_counts, int fetch) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    pdl_launch_dependents();  // the fetch grid may start now; it synchronizes per request
+    // Flags are raised only when a fetch grid follows: it advances the epoch, so flags
+    // left by earlier calls never equal the value a later fetch waits for.
+    const bool pub = fetch != 0;
+    const Plan P(L.C, L.S);
+    Request R(L, P, smem, sel, k, out);
+    const uint32_t ready = ld_relaxed(L.epoch + R.b) + 1u;
+    // ready_pos carries the call's tag in its high half and the miss count in its low
+    // half, so a fetch CTA learns both from the one acquire load it waits on.
+    const uint32_t tag = (ready & 0xffffu) << 16;
+    uint32_t* rpos = L.ready_pos + R.b;
+    uint32_t* rslot = L.ready_slot + R.b;
+    if (!R.begin(miss_counts)) {  // refused: nothing to fetch for this request
+        if (pub && threadIdx.x == 0) st_release(rpos, tag);
         return;
     }
-
-    // ---- 1. hit detection: probe the page table, four selections per thread in flight
-    uint32_t st = 0;
-    int any_miss = 0;
-    for (int j0 = 0; j0 < k; j0 += 4 * NT) {
-        int32_t p[4], s[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int j = j0 + q * NT + tid;
-            p[q] = j < k ? __ldg(selb + j) : -1;
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) s[q] = (p[q] >= 0 && p[q] < C) ? ptb[p[q]] : -1;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int j = j0 + q * NT + tid;
-            if (j >= k) continue;
-            const int32_t pp = p[q], ss = s[q];
-            if (ss >= 0) {  // hit: answered in place, stamped, not evictable
-                const uint32_t bit = 1u << (ss & 31);
-                if (atomicOr(&hitbm[ss >> 5], bit) & bit) st |= HS_STATUS_DUP;
-                lub[ss] = t;
-                outb[j] = ss;
-            } else if (pp >= 0 && pp < C) {  // miss
-                const uint32_t bit = 1u << (pp & 31);
-                if (atomicOr(&posbm[pp >> 5], bit) & bit) st |= HS_STATUS_DUP;
-                any_miss = 1;
-            } else {  // padding, or out of range
-                if (pp >= C) st |= HS_STATUS_RANGE;
-                outb[j] = -1;
-            }
-        }
-    }
-    if (st) atomicOr(L.status, st);
-    if (!__syncthreads_or(any_miss)) {  // all hits: nothing to rank or fetch
-        if (tid == 0) {
-            miss_counts[b] = 0;
-            L.mcnt[b] = 0;
-            L.step[b] = t + 1;
-        }
+    if (!R.probe()) {  // all hits: nothing to rank or fetch
+        if (pub && threadIdx.x == 0) st_release(rpos, tag);
+        R.finish(miss_counts, 0);
         return;
     }
+    R.rank_misses();
+    R.export_misses();
+    publish(rpos, tag | R.m, pub);  // the fetch of this request's rows can start
+    R.rank_victims();
+    R.apply();
+    publish(rslot, ready, pub);  // ... and its rows can be stored
+    R.answer_misses();
+    R.finish(miss_counts, R.m);
+}
 
-    // ---- 2. count misses per bitmap group and non-hit slots per hit-bitmap word
-    const int gpt = (P.CG + NT - 1) / NT;
-    const int g0 = min(tid * gpt, P.CG), g1 = min(g0 + gpt, P.CG);
-    const int wpt = (P.SW + NT - 1) / NT;
-    const int w0 = min(tid * wpt, P.SW), w1 = min(w0 + wpt, P.SW);
-    const uint32_t tail_mask = (S & 31) ? ((1u << (S & 31)) - 1u) : 0xffffffffu;
-
-    for (int s = tid; s < S; s += NT) keys[s] = (uint32_t)(lub[s] + 1);
-
-    uint32_t nmiss = 0, ncand = 0;
-    for (int g = g0; g < g1; ++g)
+// One fetch CTA's share of request b: rows q, q + nq, q + 2nq, ... of its m misses.
+__device__ __forceinline__ void fetch_rows(const Layout& L, int b, uint32_t q, uint32_t nq, uint32_t ready,
+                                           uint32_t* bcast) {
+    constexpr int GT = kGatherThreads;
+    uint32_t v;
+    if (!wait_flag(L.ready_pos + b, (ready & 0xffffu) << 16, 0xffff0000u, L.status, bcast, &v)) return;
+    const uint32_t m = v & 0xffffu;
+    const uint32_t cpr = (uint32_t)L.E >> 4;
+    const uint32_t rows = m > q ? (m - q + nq - 1) / nq : 0u;
+    const uint32_t n = rows * cpr;
+    const int32_t* gpos = L.mpos + (size_t)b * L.S;
+    const int32_t* gslot = L.mslot + (size_t)b * L.S;
+    const uint8_t* hb = L.host + (size_t)b * L.C * L.host_stride;
+    uint8_t* db = L.dev + (size_t)b * L.S * L.E;
+    bool slots_known = false;
+    for (uint32_t base = 0; base < n; base += GT * kGatherUnroll) {
+        uint4 val[kGatherUnroll];
 #pragma unroll
-        for (int q = 0; q < kGroupWords; ++q) nmiss += __popc(posbm[g * kGroupWords + q]);
-    for (int w = w0; w < w1; ++w) ncand += __popc(~hitbm[w] & (w == P.SW - 1 ? tail_mask : 0xffffffffu));
-
-    // one scan for both counts: misses in the low 16 bits, candidates in the high 16
-    uint32_t total;
-    const uint32_t excl = block_exclusive_scan<NT>((ncand << 16) | nmiss, scratch, &total);
-    const uint32_t m = total & 0xffffu, N = total >> 16;
-    const uint32_t miss_base = excl & 0xffffu;
-
-    {
-        uint32_t r = miss_base;
-        for (int g = g0; g < g1; ++g) {
-            gprefix[g] = r;
-#pragma unroll
-            for (int q = 0; q < kGroupWords; ++q) r += __popc(posbm[g * kGroupWords + q]);
+        for (int u = 0; u < kGatherUnroll; ++u) {
+            const uint32_t c = base + (uint32_t)u * GT + threadIdx.x;
+            if (c < n) {
+                const uint32_t lr = c / cpr, off = c - lr * cpr;
+                const int32_t p = __ldcg(gpos + q + nq * lr);
+                val[u] = __ldcs(reinterpret_cast<const uint4*>(hb + (size_t)p * L.host_stride) + off);
+            }
         }
-    }
-
-    // ---- 3. non-hit slots in slot order, and the range of their keys
-    uint32_t kmin = 0xffffffffu, kmax = 0u;
-    {
-        uint32_t c = excl >> 16;
-        for (int w = w0; w < w1; ++w) {
-            uint32_t bits = ~hitbm[w] & (w == P.SW - 1 ? tail_mask : 0xffffffffu);
-            while (bits) {
-                const int s = w * 32 + __ffs(bits) - 1;
-                bits &= bits - 1;
-                sa[c++] = (uint16_t)s;
-                const uint32_t key = keys[s];
-                kmin = min(kmin, key);
-                kmax = max(kmax, key);
+        if (!slots_known) {  // the loads above are in flight while the victims are ranked
+            if (!wait_flag(L.ready_slot + b, ready, 0xffffffffu, L.status, bcast, &v)) return;
+            slots_known = true;
+        }
+#pragma unroll
+        for (int u = 0; u < kGatherUnroll; ++u) {
+            const uint32_t c = base + (uint32_t)u * GT + threadIdx.x;
+            if (c < n) {
+                const uint32_t lr = c / cpr, off = c - lr * cpr;
+                const int32_t v = __ldcg(gslot + q + nq * lr);
+                reinterpret_cast<uint4*>(db + (size_t)v * L.E)[off] = val[u];
             }
         }
     }
-    kmin = __reduce_min_sync(0xffffffffu, kmin);
-    kmax = __reduce_max_sync(0xffffffffu, kmax);
-    if (lane == 0) {
-        scratch[warp] = kmin;
-        scratch[kResolveWarps + warp] = kmax;
-    }
+}
+
+// Request b's fetch by nq CTAs (this one is share q); the last of them to finish
+// closes the request's call by advancing its epoch.
+__device__ __forceinline__ void fetch_request(const Layout& L, int b, uint32_t q, uint32_t nq, uint32_t* bcast) {
+    const uint32_t ready = ld_relaxed(L.epoch + b) + 1u;
+    fetch_rows(L, b, q, nq, ready, bcast);
     __syncthreads();
-    if (tid == 0) {
-        uint32_t a = scratch[0], z = scratch[kResolveWarps];
-        for (int i = 1; i < kResolveWarps; ++i) {
-            a = min(a, scratch[i]);
-            z = max(z, scratch[kResolveWarps + i]);
+    if (threadIdx.x == 0) {
+        if (nq == 1u || atomicAdd(L.done + b, 1u) == nq - 1u) {
+            if (nq > 1u) L.done[b] = 0u;
+            st_release(L.epoch + b, ready);
         }
-        scratch[2 * kResolveWarps] = a;
-        scratch[2 * kResolveWarps + 1] = z;
-    }
-    __syncthreads();
-    kmin = scratch[2 * kResolveWarps];
-    kmax = scratch[2 * kResolveWarps + 1];
-    __syncthreads();  // scratch is reused by the scans below
-
-    // ---- 4. LRU order: stable LSD radix sort of the candidates on last_use + 1
-    const uint32_t range = kmax - kmin;
-    const int npass = range ? (32 - __clz(range) + kRadixBits - 1) / kRadixBits : 0;
-    const int seg = (((int)N + kResolveWarps - 1) / kResolveWarps + 31) & ~31;
-    const int s0 = min(warp * seg, (int)N), s1 = min(s0 + seg, (int)N);
-    uint16_t* src = sa;
-    uint16_t* dst = sb;
-    for (int pass = 0; pass < npass; ++pass) {
-        const int shift = pass * kRadixBits;
-        for (int i = tid; i < kBins * kResolveWarps; i += NT) counts[i] = 0u;
-        __syncthreads();
-        for (int base = s0; base < s1; base += 32) {
-            const int idx = base + lane;
-            const bool v = idx < s1;
-            const uint32_t d = v ? ((keys[src[idx]] - kmin) >> shift) & (kBins - 1) : (uint32_t)kBins;
-            const uint32_t peers = __match_any_sync(0xffffffffu, d);
-            if (v && lane == __ffs(peers) - 1) counts[d * kResolveWarps + warp] += __popc(peers);
-        }
-        __syncthreads();
-        {
-            constexpr int PER = kBins * kResolveWarps / NT;
-            uint32_t loc[PER], sum = 0;
-#pragma unroll
-            for (int q = 0; q < PER; ++q) {
-                loc[q] = counts[tid * PER + q];
-                sum += loc[q];
-            }
-            uint32_t tot;
-            uint32_t ex = block_exclusive_scan<NT>(sum, scratch, &tot);
-#pragma unroll
-            for (int q = 0; q < PER; ++q) {
-                counts[tid * PER + q] = ex;
-                ex += loc[q];
-            }
-        }
-        __syncthreads();
-        for (int base = s0; base < s1; base += 32) {
-            const int idx = base + lane;
-            const bool v = idx < s1;
-            const uint16_t sl = v ? src[idx] : (uint16_t)0;
-            const uint32_t d = v ? ((keys[sl] - kmin) >> shift) & (kBins - 1) : (uint32_t)kBins;
-            const uint32_t peers = __match_any_sync(0xffffffffu, d);
-            if (v) dst[counts[d * kResolveWarps + warp] + __popc(peers & lanemask_lt())] = sl;
-            __syncwarp();
-            if (v && lane == __ffs(peers) - 1) counts[d * kResolveWarps + warp] += __popc(peers);
-            __syncwarp();
-        }
-        __syncthreads();
-        uint16_t* tmp = src;
-        src = dst;
-        dst = tmp;
-    }
-    const uint16_t* victims = src;  // victims[r] = the slot the r-th miss takes
-
-    // ---- 5. misses by rank (ascending position), then unmap / map / stamp
-    uint32_t* mpos = keys;  // keys are dead after the sort
-    {
-        uint32_t r = miss_base;
-        for (int g = g0; g < g1; ++g)
-            for (int q = 0; q < kGroupWords; ++q) {
-                const int w = g * kGroupWords + q;
-                uint32_t bits = posbm[w];
-                while (bits) {
-                    mpos[r++] = (uint32_t)(w * 32 + __ffs(bits) - 1);
-                    bits &= bits - 1;
-                }
-            }
-    }
-    __syncthreads();
-    int2* mlb = L.mlist + (size_t)b * S;
-    for (uint32_t r = tid; r < m; r += NT) {
-        const int32_t p = (int32_t)mpos[r];
-        const int32_t v = victims[r];
-        const int32_t o = tokb[v];
-        if (o >= 0) ptb[o] = -1;
-        ptb[p] = v;
-        tokb[v] = p;
-        lub[v] = t;
-        mlb[r] = make_int2(p, v);
-    }
-
-    // ---- 6. answers for the missed selections
-    for (int j = tid; j < k; j += NT) {
-        const int32_t p = __ldg(selb + j);
-        if (p < 0 || p >= C) continue;
-        const int w = p >> 5;
-        const uint32_t bit = 1u << (p & 31);
-        const uint32_t word = posbm[w];
-        if (!(word & bit)) continue;  // a hit, already answered
-        const int g = w / kGroupWords;
-        uint32_t rank = gprefix[g];
-        for (int q = g * kGroupWords; q < w; ++q) rank += __popc(posbm[q]);
-        rank += __popc(word & (bit - 1u));
-        outb[j] = victims[rank];
-    }
-    if (tid == 0) {
-        miss_counts[b] = (int32_t)m;
-        L.mcnt[b] = (int32_t)m;
-        L.step[b] = t + 1;
     }
 }
 
 __global__ void __launch_bounds__(kGatherThreads, kGatherCtasPerSm)
 gather_kernel(const Layout L) {
-    constexpr int NT = kGatherThreads;
-    extern __shared__ __align__(16) uint32_t pref[];  // R + 1 row offsets, then scan scratch
-    uint32_t* scratch = pref + L.R + 1;
-    const int tid = threadIdx.x;
-    const int R = L.R;
-
-    pdl_wait_primary();  // the resolution kernel's miss list is complete and visible
-
-    const int per = (R + NT - 1) / NT;
-    const int r0 = min(tid * per, R), r1 = min(r0 + per, R);
-    uint32_t sum = 0;
-    for (int i = r0; i < r1; ++i) {
-        const uint32_t c = (uint32_t)L.mcnt[i];
-        pref[i] = c;
-        sum += c;
-    }
-    uint32_t total;
-    uint32_t ex = block_exclusive_scan<NT>(sum, scratch, &total);
-    for (int i = r0; i < r1; ++i) {
-        const uint32_t c = pref[i];
-        pref[i] = ex;
-        ex += c;
-    }
-    __syncthreads();
-
-    const uint32_t cpr = (uint32_t)L.E >> 4;  // 16-byte chunks per row
-    const uint32_t nchunks = total * cpr;
-    const uint32_t T = gridDim.x * NT;
-    for (uint32_t base = blockIdx.x * NT + tid; base < nchunks; base += T * kGatherUnroll) {
-        uint4 val[kGatherUnroll];
-        uint4* dptr[kGatherUnroll];
-#pragma unroll
-        for (int u = 0; u < kGatherUnroll; ++u) {
-            const uint32_t c = base + (uint32_t)u * T;
-            dptr[u] = nullptr;
-            if (c < nchunks) {
-                const uint32_t row = c / cpr, off = c - row * cpr;
-                int lo = 0, hi = R - 1;  // the request: last b with pref[b] <= row
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (pref[mid] <= row) lo = mid; else hi = mid - 1;
-                }
-                const int2 e = L.mlist[(size_t)lo * L.S + (row - pref[lo])];
-                const uint4* s = reinterpret_cast<const uint4*>(
-                                     L.host + ((size_t)lo * L.C + (uint32_t)e.x) * L.host_stride) + off;
-                dptr[u] = reinterpret_cast<uint4*>(L.dev + ((size_t)lo * L.S + (uint32_t)e.y) * L.E) + off;
-                val[u] = __ldcs(s);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kGatherUnroll; ++u)
-            if (dptr[u]) *dptr[u] = val[u];
+    __shared__ uint32_t bcast[2];
+    const uint32_t G = gridDim.x, c = blockIdx.x, R = (uint32_t)L.R;
+    if (G >= R) {  // several CTAs share each request
+        const uint32_t b = c % R;
+        fetch_request(L, (int)b, c / R, (G - 1 - b) / R + 1, bcast);
+    } else {  // each CTA takes whole requests
+        for (uint32_t b = c; b < R; b += G) fetch_request(L, (int)b, 0, 1, bcast);
     }
 }
 
 }  // namespace
 
-size_t resolve_smem_bytes(int C, int S) { return SmemPlan(C, S).bytes(S); }
+size_t resolve_smem_bytes(int C, int S) { return Plan(C, S).fixed; }
 
-size_t gather_smem_bytes(int R) { return (size_t)(R + 1 + kGatherThreads / 32 + 1) * 4; }
+size_t gather_smem_bytes() { return 0; }
+
+size_t miss_area_bytes(int R, int S) {
+    const size_t list = ((size_t)R * S * 4 + 15) & ~(size_t)15;
+    const size_t per = ((size_t)R * 4 + 15) & ~(size_t)15;
+    return 2 * list + 4 * per;
+}
+
+void carve_miss_area(Layout& L, void* base) {
+    uint8_t* p = static_cast<uint8_t*>(base);
+    const size_t list = ((size_t)L.R * L.S * 4 + 15) & ~(size_t)15;
+    const size_t per = ((size_t)L.R * 4 + 15) & ~(size_t)15;
+    L.mpos = reinterpret_cast<int32_t*>(p);
+    L.mslot = reinterpret_cast<int32_t*>(p + list);
+    p += 2 * list;
+    L.ready_pos = reinterpret_cast<uint32_t*>(p);
+    L.ready_slot = reinterpret_cast<uint32_t*>(p + per);
+    L.epoch = reinterpret_cast<uint32_t*>(p + 2 * per);
+    L.done = reinterpret_cast<uint32_t*>(p + 3 * per);
+}
 
 cudaError_t configure_kernels(int device) {
     // The attribute is per kernel, not per context: opt in to the device maximum once,
@@ -421,15 +576,13 @@ cudaError_t configure_kernels(int device) {
     int optin = 0;
     cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    return cudaFuncSetAttribute(resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
 }
 
 cudaError_t launch_resolve(const Layout& L, cudaStream_t stream, const int32_t* sel, int k,
-                           int32_t* out_slots, int32_t* miss_counts) {
+                           int32_t* out_slots, int32_t* miss_counts, bool fetch) {
     resolve_kernel<<<L.R, kResolveThreads, resolve_smem_bytes(L.C, L.S), stream>>>(L, sel, k, out_slots,
-                                                                                   miss_counts);
+                                                                                   miss_counts, fetch ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -437,7 +590,7 @@ cudaError_t launch_gather(const Layout& L, cudaStream_t stream, int num_sms, boo
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(num_sms * kGatherCtasPerSm));
     cfg.blockDim = dim3(kGatherThreads);
-    cfg.dynamicSmemBytes = gather_smem_bytes(L.R);
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

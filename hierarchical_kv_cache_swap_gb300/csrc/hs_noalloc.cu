@@ -19,7 +19,8 @@
 
 namespace {
 
-// [R][S] int2 miss list, then [R] miss counts, then one status word.
+// The miss area of the two kernels (positions, slots, counts, per-request flags, the
+// call epoch), then one status word. Zero at load, which is a valid initial state.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[HS_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
@@ -69,23 +70,22 @@ extern "C" int hs_resolve_noalloc(hs_stream_t stream, int num_requests, int cont
         ((uintptr_t)device_kv & 15))
         return noalloc_fail(HS_ERR_INVALID,
                             "host_kv/device_kv must be 16-byte aligned and host_stride a multiple of 16 >= entry_bytes");
-    if (S > hs::kMaxSlots || R > hs::kMaxRequestsGather)
+    if (S > hs::kMaxSlots || R > hs::kMaxRequests)
         return noalloc_fail(HS_ERR_LIMIT, "slots or num_requests beyond this build's limits");
     if ((unsigned long long)R * S * (E / 16) > (1ull << 31))
         return noalloc_fail(HS_ERR_LIMIT, "device buffer beyond 32 GiB");
-    const size_t list_bytes = sizeof(int2) * (size_t)R * S;
-    const size_t need = list_bytes + sizeof(int32_t) * (size_t)R + sizeof(uint32_t);
-    if (need > HS_NOALLOC_SCRATCH_BYTES)
+    const size_t area = hs::miss_area_bytes(R, S);
+    if (area + sizeof(uint32_t) > HS_NOALLOC_SCRATCH_BYTES)
         return noalloc_fail(HS_ERR_LIMIT,
                             "num_requests * slots too large for the fixed scratch array "
-                            "(8*R*S + 4*R + 4 bytes must fit in HS_NOALLOC_SCRATCH_BYTES)");
+                            "(about 8*R*S + 16*R bytes must fit in HS_NOALLOC_SCRATCH_BYTES)");
     int dev = -1, optin = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return noalloc_fail(HS_ERR_CUDA, cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return noalloc_fail(HS_ERR_LIMIT, "device ordinal beyond 63");
     if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
         return noalloc_fail(HS_ERR_CUDA, cudaGetErrorString(e));
-    if (hs::resolve_smem_bytes(C, S) > (size_t)optin || hs::gather_smem_bytes(R) > (size_t)optin)
+    if (hs::resolve_smem_bytes(C, S) > (size_t)optin)
         return noalloc_fail(HS_ERR_LIMIT, "context_len/slots need more shared memory than a CTA has");
     DeviceSetup* d = nullptr;
     if ((e = setup_device(dev, &d)) != cudaSuccess) return noalloc_fail(HS_ERR_CUDA, cudaGetErrorString(e));
@@ -100,13 +100,12 @@ extern "C" int hs_resolve_noalloc(hs_stream_t stream, int num_requests, int cont
     L.tok = slot_token;
     L.lu = last_use;
     L.step = step;
-    L.mlist = reinterpret_cast<int2*>(base);
-    L.mcnt = reinterpret_cast<int32_t*>(base + list_bytes);
-    L.status = status ? status : reinterpret_cast<uint32_t*>(base + list_bytes + sizeof(int32_t) * (size_t)R);
+    hs::carve_miss_area(L, base);
+    L.status = status ? status : reinterpret_cast<uint32_t*>(base + area);
     cudaStream_t s = (cudaStream_t)stream;
-    if ((e = hs::launch_resolve(L, s, selections, k, out_slots, miss_counts)) != cudaSuccess)
+    if ((e = hs::launch_resolve(L, s, selections, k, out_slots, miss_counts, true)) != cudaSuccess)
         return noalloc_fail(HS_ERR_CUDA, cudaGetErrorString(e));
-    if ((e = hs::launch_gather(L, s, d->num_sms, true)) != cudaSuccess)
+    if ((e = hs::launch_gather(L, s, d->num_sms, hs::overlap_fetch(R, d->num_sms))) != cudaSuccess)
         return noalloc_fail(HS_ERR_CUDA, cudaGetErrorString(e));
     hs::record_error("");
     return HS_OK;

@@ -17,7 +17,8 @@
  *   slot tokens     int32 [R][S]: slot -> position, -1 when empty;
  *   last use        int32 [R][S]: per-slot recency stamp, -1 when never used;
  *   step            int32 [R]: calls made so far per request (the stamp of the next call);
- *   a miss list and a device status word (internal).
+ *   a miss area (miss lists and the flags that let the two kernels of a call
+ *   overlap) and a device status word (internal).
  * R = num_requests, C = context_len, S = slots. Everything starts empty: page
  * table, slot tokens and last use at -1, step 0, device buffer zero.
  *
@@ -63,6 +64,7 @@ typedef struct CUevent_st* hs_event_t;
 #define HS_STATUS_RANGE 1u    /* a selection was >= context_len */
 #define HS_STATUS_DUP 2u      /* a position appeared twice in one request's row */
 #define HS_STATUS_STEP_LIMIT 4u /* a request reached 2^31-1 calls; the call was skipped */
+#define HS_STATUS_TIMEOUT 8u    /* a fetch waited too long for its resolution (should not happen) */
 
 /* flags (hs_set_flags) */
 #define HS_FLAG_NO_COPY 1u /* do all bookkeeping but skip the host->device row fetch */
@@ -75,8 +77,8 @@ typedef struct CUevent_st* hs_event_t;
  *   slots         S > 0 device slots per request (the GPU cache size)
  *   entry_bytes   E > 0 bytes per KV entry; a multiple of 16
  * Uses the calling thread's current CUDA device. Allocates everything up front
- * (R*C*E bytes of pinned host memory, R*S*E bytes of HBM, 4*R*(C+3S+1) bytes of
- * tables); hs_resolve allocates nothing. Returns NULL on failure (HS_ERR_INVALID,
+ * (R*C*E bytes of pinned host memory, R*S*E bytes of HBM, about 4*R*(C+6S+5) bytes of
+ * tables, miss lists and staging); hs_resolve allocates nothing. Returns NULL on failure (HS_ERR_INVALID,
  * HS_ERR_LIMIT, HS_ERR_NOMEM or HS_ERR_CUDA described by hs_last_error()). The caller
  * owns the handle and releases it with hs_destroy.
  */
@@ -115,9 +117,10 @@ int hs_resolve_host(hs_ctx* ctx, hs_stream_t stream, const int32_t* selections_h
 
 /*
  * hs_resolve_profiled -- hs_resolve that records ev[0] before the resolution kernel,
- * ev[1] between it and the fetch kernel, and ev[2] after the fetch (for per-kernel
- * timing). The two kernels are then not overlapped. ev entries must be valid events
- * created on the context's device. Results are identical to hs_resolve.
+ * ev[1] between it and the fetch kernel and ev[2] after the fetch (per-kernel timing
+ * with events on the launching stream). The two kernels then run one after the other
+ * instead of overlapping. ev entries must be valid events created on the context's
+ * device. Results are identical to hs_resolve.
  */
 int hs_resolve_profiled(hs_ctx* ctx, hs_stream_t stream, const int32_t* selections, int B, int k,
                         int32_t* out_slots, int32_t* miss_counts, hs_event_t ev[3]);
@@ -179,12 +182,14 @@ const char* hs_last_error(void);
  *   status        device uint32 that collects HS_STATUS_* bits, or NULL
  * It allocates nothing and calls no allocating routine. The miss list the two kernels
  * share lives in a fixed file-scope device array of HS_NOALLOC_SCRATCH_BYTES bytes,
- * which every GPU that loads this library keeps until the process exits; calls need
- * 8*R*S + 4*R + 4 bytes of it and larger sizes fail with HS_ERR_LIMIT before anything
- * is enqueued. Every call on a device shares that device's copy of the array, so calls
+ * which every GPU that loads this library keeps until the process exits; a call needs
+ * about 8*R*S + 16*R bytes of it (up to 96 more for alignment) and larger sizes fail with
+ * HS_ERR_LIMIT before anything is enqueued. Every call on a device shares that device's copy of the array, so calls
  * whose work overlaps on the GPU (on two streams, say) race: serialise them. The array
- * keeps the last call's contents; every call writes what it later reads, so nothing in
- * it needs clearing between calls. The first call on a
+ * keeps the last call's contents, which the next call continues from: besides the
+ * lists every call rewrites, it holds per-request flags and a call counter that the
+ * two kernels use to find each other's results; it starts zeroed at load, which is a
+ * valid state, and needs no clearing between calls. The first call on a
  * device does a one-time set-up with that device current (it looks up the array's
  * device address and sets kernel attributes): make that first call before any stream
  * capture. Returns HS_OK or HS_ERR_* (hs_last_error() describes it).

@@ -51,7 +51,7 @@ def test_create_rejects_bad_sizes_before_touching_cuda(lib):
     assert "multiple of 16" in hs.last_error()
     assert not lib.hs_create(1, 8, 70000, 16)
     assert "exceeds" in hs.last_error()
-    assert not lib.hs_create(20000, 8, 8, 16)
+    assert not lib.hs_create(2_000_000, 8, 8, 16)
     assert "exceeds" in hs.last_error()
     assert not lib.hs_create(1 << 14, 1 << 10, 1 << 14, 1 << 12)
     assert "32 GiB" in hs.last_error()
