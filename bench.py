@@ -53,6 +53,25 @@ def workload_for_rank(name: str, rank: int):
     return w if rank == 0 else replace(w, seed=w.seed + 7919 * rank)
 
 
+def profiled_traffic(kernel: str, workload: str):
+    """ncu figures recorded in profiles/<kernel>_<workload>.md, or None once the kernel
+    source has changed since the capture (its sha256 is recorded beside them)."""
+    import hashlib
+    import re
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    src = os.path.join(ROOT, "hierarchical_kv_cache_swap_gb300", "csrc", "hs_kernels.cu")
+    try:
+        text = open(path).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    m = re.search(r"```json\n(.*?)```", text, re.S)
+    if not m:
+        return None
+    fig = json.loads(m.group(1))
+    return fig if fig.get("kernel_source_sha256") == digest else None
+
+
 def reduce_max(values, dist, device):
     """Element-wise max of `values` over all ranks (identity without a process group)."""
     if dist is None:
@@ -324,8 +343,15 @@ def run_ours(args, rank: int, world: int, dist) -> None:
         "overlap_saving_us_per_step": (res_total + gat_total - total_ms) / K * 1e3,
     }
     if gat_total >= res_total:
+        fig = profiled_traffic("gather_kernel", w.name)
+        per_launch = miss_bytes / K
         roofline = {"bound": "h2d_link", "kernel": "gather_kernel", "achieved": fetch_gbs_kernel,
-                    "peak": peak_h2d, "unit": "GB/s", "frac": fetch_gbs_kernel / peak_h2d, "traffic": None,
+                    "peak": peak_h2d, "unit": "GB/s", "frac": fetch_gbs_kernel / peak_h2d,
+                    "traffic": fig and fig["dram_bytes_per_algorithmic_link_byte"] * per_launch,
+                    "link_traffic": fig and fig["link_bytes_per_algorithmic_link_byte"] * per_launch,
+                    "algorithmic_bytes_per_launch": per_launch,
+                    "traffic_source": "profiles/gather_kernel_dsa.md (ncu, scaled to this run's mean misses)"
+                    if fig else None,
                     "peak_source": "pinned cudaMemcpyAsync host->device, 1 GiB, best of 10, this run"}
     else:
         a_ = res_bytes / (res_total * 1e-3) / 1e9
