@@ -388,6 +388,97 @@ def run_ours(args, rank: int, world: int, dist) -> None:
     print(json.dumps(line), flush=True)
 
 
+def run_layers(args, rank: int, world: int, dist) -> None:
+    """Quest-style pages, 8 layers sharing one selection per step: the two-stream overlap of
+    layer l+1's resolution with layer l's consumer (the checksum stand-in), against the
+    serial order and against the serial order without fetches (the miss overhead)."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    import hierarchical_kv_cache_swap_gb300 as hs
+    import tracegen
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    __graft_entry__.build()
+    w = workload_for_rank("quest", rank)
+    K, W = args.steps, args.warmup
+    T = W + K
+    B, L = w.B, w.L
+    sel = torch.from_numpy(tracegen.trace(w, T=T)).cuda()
+    lender = hs.Context(B, w.C, w.S, w.E)  # one host store lent to every layer (timing only)
+    tracegen.fill_kv(lender.host_kv_address(), lender.host_stride, w)
+    ctxs = [lender] + [hs.Context(B, w.C, w.S, w.E, share_host_with=lender) for _ in range(L - 1)]
+    out = torch.empty((L, B, w.k), dtype=torch.int32, device="cuda")
+    miss = torch.empty((T, L, B), dtype=torch.int32, device="cuda")
+    sums = torch.empty((L, B), dtype=torch.int64, device="cuda")
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    s_res, s_use = torch.cuda.Stream(), torch.cuda.Stream()
+    peak_h2d = h2d_peak_gbs(torch)
+
+    def run(mode):
+        for c in ctxs:
+            c.reset()
+            c.set_flags(hs.HS_FLAG_NO_COPY if mode == "serial_no_fetch" else 0)
+        torch.cuda.synchronize()
+        times = []
+        for t in range(T):
+            timed = t >= W
+            flush.fill_(t & 0xFF)
+            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s_res.wait_stream(torch.cuda.current_stream())
+            s_use.wait_stream(torch.cuda.current_stream())
+            a.record(s_res)
+            for layer in range(L):
+                ctxs[layer].resolve(sel[t], out[layer], miss[t, layer], stream=s_res)
+                if mode == "overlap":
+                    ev = torch.cuda.Event()
+                    ev.record(s_res)
+                    s_use.wait_event(ev)
+                    ctxs[layer].checksum_rows(out[layer], sums[layer], stream=s_use)
+                else:
+                    ctxs[layer].checksum_rows(out[layer], sums[layer], stream=s_res)
+            if mode == "overlap":
+                s_res.wait_stream(s_use)
+            z.record(s_res)
+            torch.cuda.current_stream().wait_stream(s_res)
+            if timed:
+                times.append((a, z))
+        torch.cuda.synchronize()
+        return [x.elapsed_time(y) * 1e3 for x, y in times]
+
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as sampler:
+        res = {m: run(m) for m in ("serial", "overlap", "serial_no_fetch")}
+    status = lender.status()
+    miss_rows = float(miss[W:].sum())
+    for c in reversed(ctxs):
+        c.close()
+    med = {m: statistics.median(v) for m, v in res.items()}
+    tot = {m: sum(v) for m, v in res.items()}
+    overhead = tot["serial"] - tot["serial_no_fetch"]
+    value = weak_scaling_value(world, B * L, K, tot["overlap"] / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT + " (request-layer)", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": tot["overlap"] / K / 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+        "config": {"workload": describe(w) + f"; one selection shared by the {L} layers; the layers' "
+                   "contexts share one host store (timing only)",
+                   "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MiB write)"},
+        "layerwise_prefetch": {
+            "us_per_step": {m: tot[m] / K for m in tot}, "us_per_step_median": med,
+            "us_per_layer_step_overlapped": tot["overlap"] / K / L,
+            "miss_overhead_us_per_step": overhead / K,
+            "hidden_fraction_of_miss_overhead": (tot["serial"] - tot["overlap"]) / overhead if overhead > 0 else None,
+            "miss_bytes_per_step": miss_rows * w.E / K,
+            "miss_fetch_gbs_overlapped": miss_rows * w.E / (tot["overlap"] * 1e-6) / 1e9,
+            "h2d_peak_gbs": peak_h2d,
+            "consumer_bytes_per_step": B * L * w.k * w.E},
+        "device_status": status, "clocks": sampler.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def measure_noio(torch, hs, tracegen, flush) -> dict:
     w = tracegen.noio_workload(4096)
     N = 64
@@ -467,6 +558,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
+        elif args.workload == "quest":
+            run_layers(args, rank, world, dist)
         else:
             run_ours(args, rank, world, dist)
     finally:

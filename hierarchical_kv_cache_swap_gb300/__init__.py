@@ -33,6 +33,8 @@ HS_FLAG_NO_COPY = 1
 _VP, _I, _SZ, _U = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint
 SIGNATURES = {
     "hs_create": (_VP, [_I, _I, _I, _I]),
+    "hs_create_with_host": (_VP, [_I, _I, _I, _I, _VP, _SZ]),
+    "hs_checksum_rows": (_I, [_VP, _VP, _VP, _I, _I, _VP]),
     "hs_resolve": (_I, [_VP, _VP, _VP, _I, _I, _VP, _VP]),
     "hs_resolve_host": (_I, [_VP, _VP, _VP, _I, _I, _VP, _VP]),
     "hs_resolve_profiled": (_I, [_VP, _VP, _VP, _I, _I, _VP, _VP, _VP]),
@@ -121,10 +123,19 @@ class _DeviceArray:
 class Context:
     """One layer's cache for R requests (``hs_create``); release with close()."""
 
-    def __init__(self, num_requests: int, context_len: int, slots: int, entry_bytes: int):
+    def __init__(self, num_requests: int, context_len: int, slots: int, entry_bytes: int,
+                 share_host_with: "Context | None" = None):
+        """share_host_with: borrow another context's host store (hs_create_with_host);
+        that context must outlive this one."""
         self._lib = load_library()
         self.R, self.C, self.S, self.E = num_requests, context_len, slots, entry_bytes
-        self._h = self._lib.hs_create(num_requests, context_len, slots, entry_bytes)
+        if share_host_with is None:
+            self._h = self._lib.hs_create(num_requests, context_len, slots, entry_bytes)
+        else:
+            self._lender = share_host_with
+            self._h = self._lib.hs_create_with_host(num_requests, context_len, slots, entry_bytes,
+                                                    share_host_with.host_kv_address(),
+                                                    share_host_with.host_stride)
         if not self._h:
             raise HsError(f"hs_create failed: {last_error()}")
         self.host_stride = int(self._lib.hs_host_stride(self._h))
@@ -176,6 +187,13 @@ class Context:
         self._check(self._lib.hs_resolve_profiled(self._h, _stream(stream), _addr(selections), B, k,
                                                   _addr(out_slots), _addr(miss_counts), arr),
                     "hs_resolve_profiled")
+
+    def checksum_rows(self, out_slots, sums, stream=None) -> None:
+        """Consumer stand-in: sums[b] = sum mod 2^64 of the 8-byte words of request b's
+        resolved rows (out_slots int32 [R, k], sums a 64-bit tensor [R], device)."""
+        B, k = out_slots.shape
+        self._check(self._lib.hs_checksum_rows(self._h, _stream(stream), _addr(out_slots), B, k,
+                                               _addr(sums)), "hs_checksum_rows")
 
     def reset(self, stream=None) -> None:
         self._check(self._lib.hs_reset(self._h, _stream(stream)), "hs_reset")

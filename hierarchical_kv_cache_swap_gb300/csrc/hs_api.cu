@@ -22,6 +22,7 @@ struct hs_ctx {
     int num_sms;
     unsigned flags;
     uint8_t* host_kv;      // host address of the pinned, mapped store
+    bool owns_host;        // false when the caller lent the store (hs_create_with_host)
     void* miss_area;       // miss lists, counts and flags shared by the two kernels
     int32_t* stage_sel;    // [R][S] staging for hs_resolve_host
     int32_t* stage_out;    // [R][S]
@@ -46,7 +47,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 void free_ctx(hs_ctx* h) {
     if (!h) return;
-    cudaFreeHost(h->host_kv);
+    if (h->owns_host) cudaFreeHost(h->host_kv);
     cudaFree(h->L.dev);
     cudaFree(h->L.pt);
     cudaFree(h->L.tok);
@@ -98,7 +99,13 @@ extern "C" {
 
 const char* hs_last_error(void) { return g_err; }
 
-hs_ctx* hs_create(int num_requests, int context_len, int slots, int entry_bytes) {
+}  // extern "C"
+
+namespace {
+
+// Shared by hs_create (host_kv == nullptr: allocate the store) and hs_create_with_host.
+hs_ctx* create(int num_requests, int context_len, int slots, int entry_bytes, uint8_t* host_kv,
+               size_t host_stride) {
     const int R = num_requests, C = context_len, S = slots, E = entry_bytes;
     if (R <= 0 || C <= 0 || S <= 0 || E <= 0) {
         fail(HS_ERR_INVALID, "all sizes must be positive (R=%d C=%d S=%d E=%d)", R, C, S, E);
@@ -151,19 +158,23 @@ hs_ctx* hs_create(int num_requests, int context_len, int slots, int entry_bytes)
     h->num_sms = sms;
     hs::Layout& L = h->L;
     L.R = R; L.C = C; L.S = S; L.E = E;
-    L.host_stride = (size_t)E;
+    L.host_stride = host_kv ? host_stride : (size_t)E;
     const size_t host_bytes = (size_t)R * C * L.host_stride;
     const size_t dev_bytes = (size_t)R * S * E;
-    void* hp = nullptr;
-    if ((e = cudaHostAlloc(&hp, host_bytes, cudaHostAllocMapped | cudaHostAllocPortable)) != cudaSuccess) {
-        fail(HS_ERR_NOMEM, "cudaHostAlloc of %zu bytes: %s", host_bytes, cudaGetErrorString(e));
-        free_ctx(h);
-        return nullptr;
+    void* hp = host_kv;
+    if (!host_kv) {
+        if ((e = cudaHostAlloc(&hp, host_bytes, cudaHostAllocMapped | cudaHostAllocPortable)) != cudaSuccess) {
+            fail(HS_ERR_NOMEM, "cudaHostAlloc of %zu bytes: %s", host_bytes, cudaGetErrorString(e));
+            free_ctx(h);
+            return nullptr;
+        }
+        h->owns_host = true;
     }
     h->host_kv = (uint8_t*)hp;
     void* hdev = nullptr;
     if ((e = cudaHostGetDevicePointer(&hdev, hp, 0)) != cudaSuccess) {
-        cuda_fail(e, "cudaHostGetDevicePointer");
+        cuda_fail(e, host_kv ? "cudaHostGetDevicePointer (the lent store must be pinned and mapped)"
+                             : "cudaHostGetDevicePointer");
         free_ctx(h);
         return nullptr;
     }
@@ -207,6 +218,37 @@ hs_ctx* hs_create(int num_requests, int context_len, int slots, int entry_bytes)
     }
     g_err[0] = 0;
     return h;
+}
+
+}  // namespace
+
+extern "C" {
+
+hs_ctx* hs_create(int num_requests, int context_len, int slots, int entry_bytes) {
+    return create(num_requests, context_len, slots, entry_bytes, nullptr, 0);
+}
+
+hs_ctx* hs_create_with_host(int num_requests, int context_len, int slots, int entry_bytes, uint8_t* host_kv,
+                            size_t host_stride) {
+    if (!host_kv || ((uintptr_t)host_kv & 15) || host_stride % 16 != 0 || host_stride < (size_t)entry_bytes ||
+        entry_bytes <= 0) {
+        fail(HS_ERR_INVALID, "host_kv must be 16-byte aligned and host_stride a multiple of 16 >= entry_bytes");
+        return nullptr;
+    }
+    return create(num_requests, context_len, slots, entry_bytes, host_kv, host_stride);
+}
+
+int hs_checksum_rows(hs_ctx* h, hs_stream_t stream, const int32_t* out_slots, int B, int k, uint64_t* sums) {
+    if (!h) return fail(HS_ERR_INVALID, "null context");
+    if (!out_slots || !sums) return fail(HS_ERR_INVALID, "null out_slots/sums");
+    if (B != h->L.R) return fail(HS_ERR_INVALID, "B=%d but the context has %d requests", B, h->L.R);
+    if (k <= 0 || k > h->L.S) return fail(HS_ERR_INVALID, "k=%d must be in [1, slots=%d]", k, h->L.S);
+    if (B > 65535) return fail(HS_ERR_LIMIT, "hs_checksum_rows handles at most 65535 requests");
+    cudaError_t e = hs::launch_checksum(h->L.dev, B, h->L.S, h->L.E, out_slots, k, (unsigned long long*)sums,
+                                        h->num_sms, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "checksum kernel launch");
+    g_err[0] = 0;
+    return HS_OK;
 }
 
 void hs_destroy(hs_ctx* h) {

@@ -67,6 +67,11 @@ cudaError_t launch_resolve(const Layout& L, cudaStream_t stream, const int32_t* 
 inline bool overlap_fetch(int R, int num_sms) { return R <= num_sms; }
 cudaError_t launch_gather(const Layout& L, cudaStream_t stream, int num_sms, bool pdl);
 
+// Enqueue the consumer stand-in: sums[b] = sum (mod 2^64) of the 8-byte words of the
+// k rows request b resolved to (slots < 0 skipped); zeroes sums first.
+cudaError_t launch_checksum(const uint8_t* dev, int R, int S, int E, const int32_t* out_slots, int k,
+                            unsigned long long* sums, int num_sms, cudaStream_t stream);
+
 // Set the calling thread's message for hs_last_error().
 void record_error(const char* msg);
 

@@ -85,6 +85,18 @@ typedef struct CUevent_st* hs_event_t;
 hs_ctx* hs_create(int num_requests, int context_len, int slots, int entry_bytes);
 
 /*
+ * hs_create_with_host -- hs_create over a host store the caller owns and lends: the
+ * caller keeps it alive (and does not free it) until hs_destroy returns. The store is
+ * [R][C] rows host_stride bytes apart (a multiple of 16, >= entry_bytes), 16-byte
+ * aligned, and must be pinned and mapped (cudaHostAlloc with cudaHostAllocMapped, or
+ * cudaHostRegister with cudaHostRegisterMapped). Several contexts may share one store
+ * (for example the layers of one model, or a pool sized by the deployment's
+ * host-to-device ratio); the library only reads it. Same errors as hs_create.
+ */
+hs_ctx* hs_create_with_host(int num_requests, int context_len, int slots, int entry_bytes,
+                            uint8_t* host_kv, size_t host_stride);
+
+/*
  * hs_resolve -- the fused per-layer swap-in resolution (paper abstract: hit
  * detection, LRU replacement and host-to-device fetches for each layer's selections;
  * blog commentary section three: the same step updates the page table).
@@ -124,6 +136,20 @@ int hs_resolve_host(hs_ctx* ctx, hs_stream_t stream, const int32_t* selections_h
  */
 int hs_resolve_profiled(hs_ctx* ctx, hs_stream_t stream, const int32_t* selections, int B, int k,
                         int32_t* out_slots, int32_t* miss_counts, hs_event_t ev[3]);
+
+/*
+ * hs_checksum_rows -- a stand-in for the sparse-attention consumer of a layer (blog
+ * commentary, section two: a resident entry takes part in the computation directly).
+ * Enqueues on `stream` a kernel that reads the k rows each request resolved to, through
+ * out_slots (device int32 [B][k] from hs_resolve; negative slots are skipped), and
+ * writes sums[b] = the sum modulo 2^64 of their 8-byte little-endian words (device
+ * uint64 [B], overwritten). Used to measure the overlap of layer l+1's resolution with
+ * layer l's consumer (paper abstract: exact layer-wise prefetching) and to check the
+ * consumer's view against the host rows. B must equal num_requests (at most 65535),
+ * 0 < k <= slots. Returns HS_OK, HS_ERR_INVALID, HS_ERR_LIMIT or HS_ERR_CUDA.
+ */
+int hs_checksum_rows(hs_ctx* ctx, hs_stream_t stream, const int32_t* out_slots, int B, int k,
+                     uint64_t* sums);
 
 /* hs_destroy -- synchronizes the device and frees everything; NULL is a no-op. */
 void hs_destroy(hs_ctx* ctx);

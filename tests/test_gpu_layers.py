@@ -1,0 +1,113 @@
+"""Layers that share one selection, resolved ahead of their consumer on a second stream.
+
+The paper abstract: for models that share selections across layers, exact layer-wise
+prefetching hides part of the remaining miss overhead, and because only KV placement
+changes, outputs are unchanged. Here every layer is its own context; layer l+1's
+resolution runs on one stream while layer l's consumer (the checksum stand-in) reads
+its rows on another. Everything must equal the serial order, and every consumer checksum
+must equal the checksum of the host rows the selections name.
+"""
+import numpy as np
+import pytest
+import torch
+
+import hierarchical_kv_cache_swap_gb300 as hs
+import tracegen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    hs.build()
+    tracegen.build()
+
+
+def host_checksums(host: np.ndarray, sel: np.ndarray) -> np.ndarray:
+    """Sum modulo 2^64 of the little-endian 8-byte words of host[b, sel[b, j]] over j (sel >= 0)."""
+    out = np.zeros(sel.shape[0], dtype=np.uint64)
+    for b in range(sel.shape[0]):
+        rows = host[b, sel[b][sel[b] >= 0]]
+        words = np.ascontiguousarray(rows).view("<u8")
+        out[b] = np.sum(words, dtype=np.uint64)  # numpy integer sums wrap modulo 2^64
+    return out
+
+
+def test_consumer_checksum_equals_host_rows():
+    w = tracegen.WORKLOADS["tiny"]
+    T = 12
+    ctx = hs.Context(w.B, w.C, w.S, w.E)
+    tracegen.fill_kv(ctx.host_kv_address(), ctx.host_stride, w)
+    host = ctx.host_kv()
+    sel = tracegen.trace(w, T=T)
+    sd = torch.from_numpy(sel).cuda()
+    out = torch.empty_like(sd)
+    miss = torch.empty((T, w.B), dtype=torch.int32, device="cuda")
+    sums = torch.empty((T, w.B), dtype=torch.int64, device="cuda")
+    for t in range(T):
+        ctx.resolve(sd[t], out[t], miss[t])
+        ctx.checksum_rows(out[t], sums[t])
+    got = sums.cpu().numpy().view(np.uint64)
+    for t in range(T):
+        assert np.array_equal(got[t], host_checksums(host, sel[t])), t
+    # padding is skipped by the consumer and resolves to -1
+    sel2 = sel[T - 1].copy()
+    sel2[0, :7] = -1
+    ctx.resolve(torch.from_numpy(sel2).cuda(), out[0], miss[0])
+    ctx.checksum_rows(out[0], sums[0])
+    assert np.array_equal(sums[0].cpu().numpy().view(np.uint64), host_checksums(host, sel2))
+    ctx.close()
+
+
+def test_layerwise_prefetch_on_two_streams_equals_serial():
+    w = tracegen.WORKLOADS["quest"]
+    B, L, T = 4, w.L, 10
+    sel = tracegen.trace(w, T=T, B=B)
+    sd = torch.from_numpy(sel).cuda()
+    serial = []
+    for layer in range(L):
+        c = hs.Context(B, w.C, w.S, w.E)
+        tracegen.fill_kv(c.host_kv_address(), c.host_stride, w, B=B, layer=layer)
+        serial.append(c)
+    # the overlapped run's contexts read the same host stores (lent, not copied)
+    over = [hs.Context(B, w.C, w.S, w.E, share_host_with=serial[layer]) for layer in range(L)]
+
+    def buffers():
+        return (torch.empty((T, L, B, w.k), dtype=torch.int32, device="cuda"),
+                torch.empty((T, L, B), dtype=torch.int32, device="cuda"),
+                torch.empty((T, L, B), dtype=torch.int64, device="cuda"))
+
+    out_s, miss_s, sum_s = buffers()
+    for t in range(T):
+        for layer in range(L):
+            serial[layer].resolve(sd[t], out_s[t, layer], miss_s[t, layer])
+            serial[layer].checksum_rows(out_s[t, layer], sum_s[t, layer])
+
+    out_o, miss_o, sum_o = buffers()
+    s_res, s_use = torch.cuda.Stream(), torch.cuda.Stream()
+    s_res.wait_stream(torch.cuda.current_stream())
+    s_use.wait_stream(torch.cuda.current_stream())
+    for t in range(T):
+        for layer in range(L):
+            over[layer].resolve(sd[t], out_o[t, layer], miss_o[t, layer], stream=s_res)
+            ev = torch.cuda.Event()
+            ev.record(s_res)
+            s_use.wait_event(ev)  # layer l's consumer waits for its resolution only
+            over[layer].checksum_rows(out_o[t, layer], sum_o[t, layer], stream=s_use)
+        done = torch.cuda.Event()
+        done.record(s_use)
+        s_res.wait_event(done)  # the next step's resolutions follow this step's consumers
+    torch.cuda.synchronize()
+    assert torch.equal(out_s, out_o) and torch.equal(miss_s, miss_o) and torch.equal(sum_s, sum_o)
+    for layer in range(L):
+        for name in ("page_table", "slot_token", "last_use", "step", "device_kv"):
+            assert torch.equal(getattr(serial[layer], name)(), getattr(over[layer], name)()), (layer, name)
+    # every layer's consumer read exactly the host rows of the shared selection
+    sums = sum_o.cpu().numpy().view(np.uint64)
+    for layer in (0, L - 1):
+        host = serial[layer].host_kv()
+        for t in (0, T - 1):
+            assert np.array_equal(sums[t, layer], host_checksums(host, sel[t])), (layer, t)
+    assert int(miss_s[1:].sum()) > 0
+    for c in over + serial:
+        c.close()
