@@ -56,6 +56,16 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
     return m;
 }
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -174,7 +184,7 @@ struct Request {
     uint32_t* posbm;    // missed positions of this call
     uint32_t* gprefix;  // misses before each group of kGroupWords bitmap words
     uint32_t* hitbm;    // slots hit in this call
-    uint32_t* keys;     // last_use + 1 of every slot
+    uint32_t* keys;     // last_use of every slot as loaded at kernel start (key = value + 1)
     int32_t* mpos;      // missed positions in ascending order (rank -> position)
     uint16_t* counts;   // radix digit counts, [digit][warp]
     uint32_t* scratch;
@@ -203,10 +213,20 @@ struct Request {
         sb = reinterpret_cast<uint16_t*>(smem + P.sb);
     }
 
-    // Reads the step and clears the bitmaps. Returns false (after answering every
-    // selection with -1) when the request's stamps would wrap.
+    // Starts the asynchronous copy of the request's last-use stamps into keys[] (they
+    // are only needed to rank victims, and arrive while the page table is probed),
+    // reads the step and clears the bitmaps. Returns false (after answering every
+    // selection with -1) when the request's stamps would wrap. Every exit path must
+    // wait for the copy (drain()).
     __device__ bool begin(int32_t* miss_counts) {
         const int tid = threadIdx.x;
+        const int S = L.S;
+        if ((S & 3) == 0 && ((uintptr_t)lub & 15) == 0) {  // 16-byte chunks when aligned
+            for (int i = tid; i < S / 4; i += NT) cp_async16(keys + 4 * i, lub + 4 * i);
+        } else {
+            for (int i = tid; i < S; i += NT) cp_async4(keys + i, lub + i);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
         t = L.step[b];
         for (int i = tid; i < P.CW; i += NT) posbm[i] = 0u;
         for (int i = tid; i < P.SW; i += NT) hitbm[i] = 0u;
@@ -217,6 +237,7 @@ struct Request {
             atomicOr(L.status, HS_STATUS_STEP_LIMIT);
             miss_counts[b] = 0;
         }
+        drain();
         return false;
     }
 
@@ -259,6 +280,8 @@ struct Request {
         return __syncthreads_or(any_miss) != 0;
     }
 
+    __device__ void drain() const { cp_async_wait_all(); }
+
     __device__ uint32_t word_mask(int w) const {
         const int S = L.S;
         return (w == P.SW - 1 && (S & 31)) ? ((1u << (S & 31)) - 1u) : 0xffffffffu;
@@ -267,14 +290,12 @@ struct Request {
     // 2. miss count and ascending-position ranks; candidate count; mpos[] filled.
     __device__ void rank_misses() {
         const int tid = threadIdx.x;
-        const int S = L.S;
         const int gpt = (P.CG + NT - 1) / NT;
         g0 = min(tid * gpt, P.CG);
         g1 = min(g0 + gpt, P.CG);
         const int wpt = (P.SW + NT - 1) / NT;
         w0 = min(tid * wpt, P.SW);
         w1 = min(w0 + wpt, P.SW);
-        for (int s = tid; s < S; s += NT) keys[s] = (uint32_t)(lub[s] + 1);
         uint32_t nmiss = 0, ncand = 0;
         for (int g = g0; g < g1; ++g)
 #pragma unroll
@@ -304,6 +325,8 @@ struct Request {
     // 4a. LRU order of the non-hit slots: ascending (last_use, slot); sets victims.
     __device__ void rank_victims() {
         const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+        drain();  // the stamps copied at kernel start have landed (this thread's part) ...
+        __syncthreads();  // ... and everyone's
         uint32_t kmin = 0xffffffffu, kmax = 0u;
         {
             uint32_t c = cand_base;
@@ -313,7 +336,7 @@ struct Request {
                     const int s = w * 32 + __ffs(bits) - 1;
                     bits &= bits - 1;
                     sa[c++] = (uint16_t)s;
-                    const uint32_t key = keys[s];
+                    const uint32_t key = keys[s] + 1u;
                     kmin = min(kmin, key);
                     kmax = max(kmax, key);
                 }
@@ -353,7 +376,7 @@ struct Request {
             for (int base = s0; base < s1; base += 32) {
                 const int idx = base + lane;
                 const bool v = idx < s1;
-                const uint32_t d = v ? ((keys[src[idx]] - kmin) >> shift) & (kBins - 1) : (uint32_t)kBins;
+                const uint32_t d = v ? ((keys[src[idx]] + 1u - kmin) >> shift) & (kBins - 1) : (uint32_t)kBins;
                 const uint32_t peers = __match_any_sync(0xffffffffu, d);
                 if (v && lane == __ffs(peers) - 1) counts[d * NW + warp] += (uint16_t)__popc(peers);
             }
@@ -380,7 +403,7 @@ struct Request {
                 const int idx = base + lane;
                 const bool v = idx < s1;
                 const uint16_t sl = v ? src[idx] : (uint16_t)0;
-                const uint32_t d = v ? ((keys[sl] - kmin) >> shift) & (kBins - 1) : (uint32_t)kBins;
+                const uint32_t d = v ? ((keys[sl] + 1u - kmin) >> shift) & (kBins - 1) : (uint32_t)kBins;
                 const uint32_t peers = __match_any_sync(0xffffffffu, d);
                 if (v) dst[counts[d * NW + warp] + __popc(peers & lanemask_lt())] = sl;
                 __syncwarp();
@@ -465,6 +488,7 @@ resolve_kernel(const Layout L, const int32_t* __restrict__ sel, int k, int32_t* 
     if (!R.probe()) {  // all hits: nothing to rank or fetch
         if (pub && threadIdx.x == 0) st_release(rpos, tag);
         R.finish(miss_counts, 0);
+        R.drain();
         return;
     }
     R.rank_misses();

@@ -57,6 +57,17 @@ def test_create_rejects_bad_sizes_before_touching_cuda(lib):
     assert "32 GiB" in hs.last_error()
 
 
+def test_lent_host_store_is_validated_before_touching_cuda(lib):
+    import ctypes
+    buf = (ctypes.c_uint8 * 4096)()
+    addr = ctypes.addressof(buf)
+    assert not lib.hs_create_with_host(1, 8, 8, 16, None, 16)
+    assert "16-byte aligned" in hs.last_error()
+    assert not lib.hs_create_with_host(1, 8, 8, 32, (addr + 15) & ~15, 16)   # stride < E
+    assert not lib.hs_create_with_host(1, 8, 8, 16, ((addr + 15) & ~15) + 8, 16)  # misaligned
+    assert lib.hs_checksum_rows(None, None, None, 1, 1, None) == hs.HS_ERR_INVALID
+
+
 def test_calls_on_null_context_fail_cleanly(lib):
     assert lib.hs_resolve(None, None, None, 1, 1, None, None) == hs.HS_ERR_INVALID
     assert lib.hs_resolve_host(None, None, None, 1, 1, None, None) == hs.HS_ERR_INVALID
