@@ -79,7 +79,7 @@ int enqueue(hs_ctx* h, cudaStream_t s, const int32_t* sel, int k, int32_t* out, 
     const bool fetch = !(h->flags & HS_FLAG_NO_COPY);
     cudaError_t e;
     if (ev && (e = cudaEventRecord(ev[0], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    if ((e = hs::launch_resolve(h->L, s, sel, k, out, miss, fetch)) != cudaSuccess)
+    if ((e = hs::launch_resolve(h->L, s, sel, k, out, miss)) != cudaSuccess)
         return cuda_fail(e, "resolution kernel launch");
     if (ev && (e = cudaEventRecord(ev[1], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     // chained by programmatic dependent launch unless events sit between the kernels
@@ -142,7 +142,7 @@ hs_ctx* create(int num_requests, int context_len, int slots, int entry_bytes, ui
         fail(HS_ERR_CUDA, "device %d cannot map host memory", dev);
         return nullptr;
     }
-    const size_t need = hs::resolve_smem_bytes(C, S);
+    const size_t need = hs::resolve_smem_bytes(C, S) + 64;  // + the kernel's static shared memory
     if (need > (size_t)smem_optin) {
         fail(HS_ERR_LIMIT, "context_len=%d / slots=%d need %zu B of shared memory per CTA (max %d)", C, S,
              need, smem_optin);

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <climits>
+
 namespace hs {
 
 constexpr int kResolveThreads = 512;               // one CTA per request
@@ -19,6 +21,7 @@ constexpr int kGatherUnroll = 8;                   // 16-byte loads in flight pe
 constexpr int kMaxSlots = 65535;                   // slot ids are kept as uint16 in shared memory
 constexpr int kMaxRequests = 1 << 20;        // requests per context
 constexpr uint32_t kSpinLimit = 1u << 21;          // bounded waits on a request's flags
+constexpr int32_t kStepLimit = INT32_MAX - 1;      // calls per request (then refused)
 
 // Everything the two kernels need about one context.
 struct Layout {
@@ -34,10 +37,8 @@ struct Layout {
     // miss area, shared by the two kernels of a call (carve_miss_area):
     int32_t* mpos;         // [R][S]: position of the r-th miss (ascending)
     int32_t* mslot;        // [R][S]: slot the r-th miss takes
-    uint32_t* ready_pos;   // [R]: ((epoch_b + 1) mod 2^16) << 16 | m_b once mpos of request b is published
-    uint32_t* ready_slot;  // [R]: == epoch_b + 1 once mslot of request b is published
-    uint32_t* epoch;       // [R]: calls of request b completed by the fetch kernel
-    uint32_t* done;        // [R]: fetch CTAs of request b finished in the current call
+    uint32_t* ready_pos;   // [R]: (step_b mod 2^16) << 16 | m_b once mpos of request b is published
+    uint32_t* ready_slot;  // [R]: == step_b once mslot of request b is published
 };
 
 // Bytes of the miss area for R requests of S slots, and its layout at `base`
@@ -53,11 +54,10 @@ size_t gather_smem_bytes();
 // device must be `device`); returns a CUDA error.
 cudaError_t configure_kernels(int device);
 
-// Enqueue the resolution kernel (one CTA per request). With `fetch` (a fetch grid is
-// launched next) it publishes each request's miss positions as soon as they are
-// ranked and the victim slots once chosen.
+// Enqueue the resolution kernel (one CTA per request). It publishes each request's
+// miss positions as soon as they are ranked and the victim slots once chosen.
 cudaError_t launch_resolve(const Layout& L, cudaStream_t stream, const int32_t* sel, int k,
-                           int32_t* out_slots, int32_t* miss_counts, bool fetch);
+                           int32_t* out_slots, int32_t* miss_counts);
 
 // Enqueue the row fetch (a persistent grid of kGatherCtasPerSm CTAs per SM). With
 // `pdl` it is chained to the preceding resolution by programmatic dependent launch and

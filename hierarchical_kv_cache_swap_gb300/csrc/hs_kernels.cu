@@ -27,8 +27,11 @@
 //   into their HBM slots. The host-link transfer -- the only real cost of the step --
 //   thus overlaps the victim ranking and the table updates, and uses every SM's load
 //   slots, not just the CTAs of the requests.
-// Flags carry the value epoch_b + 1 of the call; the last fetch CTA of request b
-// advances epoch_b, so graph replays need no host reset. Every wait is bounded: on expiry
+// Flags are tagged with the request's step after the call: the resolution advances
+// step[b] and makes it visible before it lets the fetch grid launch, so a fetch CTA
+// reads its call's tag from step[b]; every call publishes both flags, so a flag left
+// from the previous call never carries the current tag, and graph replays need no host
+// reset. Every wait is bounded: on expiry
 // the CTA records HS_STATUS_TIMEOUT and skips, so no wait can hang the GPU.
 //
 // No tensor cores: nothing here is a contraction.
@@ -82,9 +85,8 @@ __device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
 
 // All threads' global writes so far become visible before *flag = value: the barrier
 // orders them before thread 0's release store, which is cumulative. Called by every
-// thread of the CTA; a no-op when `on` is false.
-__device__ __forceinline__ void publish(uint32_t* flag, uint32_t value, bool on) {
-    if (!on) return;
+// thread of the CTA.
+__device__ __forceinline__ void publish(uint32_t* flag, uint32_t value) {
     __syncthreads();
     if (threadIdx.x == 0) st_release(flag, value);
 }
@@ -214,11 +216,9 @@ struct Request {
     }
 
     // Starts the asynchronous copy of the request's last-use stamps into keys[] (they
-    // are only needed to rank victims, and arrive while the page table is probed),
-    // reads the step and clears the bitmaps. Returns false (after answering every
-    // selection with -1) when the request's stamps would wrap. Every exit path must
-    // wait for the copy (drain()).
-    __device__ bool begin(int32_t* miss_counts) {
+    // are only needed to rank victims, and arrive while the page table is probed) and
+    // clears the bitmaps; no barrier. Every exit path must wait for the copy (drain()).
+    __device__ void start() {
         const int tid = threadIdx.x;
         const int S = L.S;
         if ((S & 3) == 0 && ((uintptr_t)lub & 15) == 0) {  // 16-byte chunks when aligned
@@ -227,35 +227,42 @@ struct Request {
             for (int i = tid; i < S; i += NT) cp_async4(keys + i, lub + i);
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
-        t = L.step[b];
         for (int i = tid; i < P.CW; i += NT) posbm[i] = 0u;
         for (int i = tid; i < P.SW; i += NT) hitbm[i] = 0u;
-        __syncthreads();
-        if (t != INT32_MAX) return true;
-        for (int j = tid; j < k; j += NT) outb[j] = -1;
-        if (tid == 0) {
+    }
+
+    // Loads the selections j0 + q*NT + tid (q < 4) and their page-table entries.
+    __device__ __forceinline__ void load_batch(int j0, int32_t (&p)[4], int32_t (&s)[4]) const {
+        const int tid = threadIdx.x;
+        const int C = L.C;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int j = j0 + q * NT + tid;
+            p[q] = j < k ? __ldg(selb + j) : -1;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) s[q] = (p[q] >= 0 && p[q] < C) ? ptb[p[q]] : -1;
+    }
+
+    // The call is refused (the request reached its call limit): every selection -1.
+    __device__ void refuse(int32_t* miss_counts) {
+        for (int j = threadIdx.x; j < k; j += NT) outb[j] = -1;
+        if (threadIdx.x == 0) {
             atomicOr(L.status, HS_STATUS_STEP_LIMIT);
             miss_counts[b] = 0;
         }
         drain();
-        return false;
     }
 
-    // 1. hit detection. Returns true (block-uniform) if any selection missed.
-    __device__ bool probe() {
+    // 1. hit detection, starting from the batch already loaded into p/s (t set).
+    // Returns true (block-uniform) if any selection missed.
+    __device__ bool probe(int32_t (&p)[4], int32_t (&s)[4]) {
         const int tid = threadIdx.x;
         const int C = L.C;
         uint32_t st = 0;
         int any_miss = 0;
         for (int j0 = 0; j0 < k; j0 += 4 * NT) {
-            int32_t p[4], s[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int j = j0 + q * NT + tid;
-                p[q] = j < k ? __ldg(selb + j) : -1;
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) s[q] = (p[q] >= 0 && p[q] < C) ? ptb[p[q]] : -1;
+            if (j0 > 0) load_batch(j0, p, s);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int j = j0 + q * NT + tid;
@@ -458,45 +465,64 @@ struct Request {
     }
 
     __device__ void finish(int32_t* miss_counts, uint32_t misses) {
-        if (threadIdx.x == 0) {
-            miss_counts[b] = (int32_t)misses;
-            L.step[b] = t + 1;
-        }
+        if (threadIdx.x == 0) miss_counts[b] = (int32_t)misses;
     }
 };
 
 __global__ void __launch_bounds__(kResolveThreads, 2)
 resolve_kernel(const Layout L, const int32_t* __restrict__ sel, int k, int32_t* __restrict__ out,
-               int32_t* __restrict__ miss_counts, int fetch) {
+               int32_t* __restrict__ miss_counts) {
     extern __shared__ __align__(16) uint8_t smem[];
-    pdl_launch_dependents();  // the fetch grid may start now; it synchronizes per request
-    // Flags are raised only when a fetch grid follows: it advances the epoch, so flags
-    // left by earlier calls never equal the value a later fetch waits for.
-    const bool pub = fetch != 0;
+    __shared__ int32_t t_sh;
+    const int b = blockIdx.x;
     const Plan P(L.C, L.S);
     Request R(L, P, smem, sel, k, out);
-    const uint32_t ready = ld_relaxed(L.epoch + R.b) + 1u;
-    // ready_pos carries the call's tag in its high half and the miss count in its low
-    // half, so a fetch CTA learns both from the one acquire load it waits on.
+    // Thread 0 advances the request's step and makes it visible GPU-wide before it lets
+    // the fetch grid launch: the new step is this call's tag on both flags (a request
+    // at its call limit keeps the saturated step and publishes "no misses"). Meanwhile
+    // the other threads start on the selections and the page table.
+    if (threadIdx.x == 0) {
+        const int32_t t0 = L.step[b];
+        L.step[b] = t0 < kStepLimit ? t0 + 1 : INT32_MAX;
+        __threadfence();
+        pdl_launch_dependents();  // the fetch grid may start; it synchronizes per request
+        t_sh = t0;
+    }
+    R.start();
+    int32_t p[4], s[4];
+    R.load_batch(0, p, s);
+    __syncthreads();  // bitmaps cleared, t_sh set
+    const int32_t t0 = t_sh;
+    const uint32_t ready = (uint32_t)(t0 < kStepLimit ? t0 + 1 : INT32_MAX);
+    // ready_pos carries the tag's low half in its high half and the miss count in its
+    // low half, so a fetch CTA learns both from the one acquire load it waits on.
     const uint32_t tag = (ready & 0xffffu) << 16;
-    uint32_t* rpos = L.ready_pos + R.b;
-    uint32_t* rslot = L.ready_slot + R.b;
-    if (!R.begin(miss_counts)) {  // refused: nothing to fetch for this request
-        if (pub && threadIdx.x == 0) st_release(rpos, tag);
+    uint32_t* rpos = L.ready_pos + b;
+    uint32_t* rslot = L.ready_slot + b;
+    if (t0 >= kStepLimit) {  // refused: nothing to fetch for this request
+        R.refuse(miss_counts);
+        if (threadIdx.x == 0) {
+            st_release(rpos, tag);
+            st_release(rslot, ready);
+        }
         return;
     }
-    if (!R.probe()) {  // all hits: nothing to rank or fetch
-        if (pub && threadIdx.x == 0) st_release(rpos, tag);
+    R.t = t0;
+    if (!R.probe(p, s)) {  // all hits: nothing to rank or fetch
+        if (threadIdx.x == 0) {
+            st_release(rpos, tag);
+            st_release(rslot, ready);
+        }
         R.finish(miss_counts, 0);
         R.drain();
         return;
     }
     R.rank_misses();
     R.export_misses();
-    publish(rpos, tag | R.m, pub);  // the fetch of this request's rows can start
+    publish(rpos, tag | R.m);  // the fetch of this request's rows can start
     R.rank_victims();
     R.apply();
-    publish(rslot, ready, pub);  // ... and its rows can be stored
+    publish(rslot, ready);  // ... and its rows can be stored
     R.answer_misses();
     R.finish(miss_counts, R.m);
 }
@@ -543,18 +569,10 @@ __device__ __forceinline__ void fetch_rows(const Layout& L, int b, uint32_t q, u
     }
 }
 
-// Request b's fetch by nq CTAs (this one is share q); the last of them to finish
-// closes the request's call by advancing its epoch.
+// Request b's fetch by nq CTAs (this one is share q), for the call tagged step[b].
 __device__ __forceinline__ void fetch_request(const Layout& L, int b, uint32_t q, uint32_t nq, uint32_t* bcast) {
-    const uint32_t ready = ld_relaxed(L.epoch + b) + 1u;
+    const uint32_t ready = ld_relaxed(reinterpret_cast<const uint32_t*>(L.step + b));
     fetch_rows(L, b, q, nq, ready, bcast);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        if (nq == 1u || atomicAdd(L.done + b, 1u) == nq - 1u) {
-            if (nq > 1u) L.done[b] = 0u;
-            st_release(L.epoch + b, ready);
-        }
-    }
 }
 
 __global__ void __launch_bounds__(kGatherThreads, kGatherCtasPerSm)
@@ -578,7 +596,7 @@ size_t gather_smem_bytes() { return 0; }
 size_t miss_area_bytes(int R, int S) {
     const size_t list = ((size_t)R * S * 4 + 15) & ~(size_t)15;
     const size_t per = ((size_t)R * 4 + 15) & ~(size_t)15;
-    return 2 * list + 4 * per;
+    return 2 * list + 2 * per;
 }
 
 void carve_miss_area(Layout& L, void* base) {
@@ -590,8 +608,6 @@ void carve_miss_area(Layout& L, void* base) {
     p += 2 * list;
     L.ready_pos = reinterpret_cast<uint32_t*>(p);
     L.ready_slot = reinterpret_cast<uint32_t*>(p + per);
-    L.epoch = reinterpret_cast<uint32_t*>(p + 2 * per);
-    L.done = reinterpret_cast<uint32_t*>(p + 3 * per);
 }
 
 cudaError_t configure_kernels(int device) {
@@ -600,13 +616,16 @@ cudaError_t configure_kernels(int device) {
     int optin = 0;
     cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, resolve_kernel)) != cudaSuccess) return e;
+    return cudaFuncSetAttribute(resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                optin - (int)fa.sharedSizeBytes);
 }
 
 cudaError_t launch_resolve(const Layout& L, cudaStream_t stream, const int32_t* sel, int k,
-                           int32_t* out_slots, int32_t* miss_counts, bool fetch) {
+                           int32_t* out_slots, int32_t* miss_counts) {
     resolve_kernel<<<L.R, kResolveThreads, resolve_smem_bytes(L.C, L.S), stream>>>(L, sel, k, out_slots,
-                                                                                   miss_counts, fetch ? 1 : 0);
+                                                                                   miss_counts);
     return cudaGetLastError();
 }
 

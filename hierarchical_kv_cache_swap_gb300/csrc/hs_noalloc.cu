@@ -19,8 +19,8 @@
 
 namespace {
 
-// The miss area of the two kernels (positions, slots, counts, per-request flags, the
-// call epoch), then one status word. Zero at load, which is a valid initial state.
+// The miss area of the two kernels (positions, slots, per-request flags), then one
+// status word. Zero at load, which is a valid initial state.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[HS_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
@@ -78,14 +78,14 @@ extern "C" int hs_resolve_noalloc(hs_stream_t stream, int num_requests, int cont
     if (area + sizeof(uint32_t) > HS_NOALLOC_SCRATCH_BYTES)
         return noalloc_fail(HS_ERR_LIMIT,
                             "num_requests * slots too large for the fixed scratch array "
-                            "(about 8*R*S + 16*R bytes must fit in HS_NOALLOC_SCRATCH_BYTES)");
+                            "(about 8*R*S + 8*R bytes must fit in HS_NOALLOC_SCRATCH_BYTES)");
     int dev = -1, optin = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return noalloc_fail(HS_ERR_CUDA, cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return noalloc_fail(HS_ERR_LIMIT, "device ordinal beyond 63");
     if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
         return noalloc_fail(HS_ERR_CUDA, cudaGetErrorString(e));
-    if (hs::resolve_smem_bytes(C, S) > (size_t)optin)
+    if (hs::resolve_smem_bytes(C, S) + 64 > (size_t)optin)  // + static shared memory
         return noalloc_fail(HS_ERR_LIMIT, "context_len/slots need more shared memory than a CTA has");
     DeviceSetup* d = nullptr;
     if ((e = setup_device(dev, &d)) != cudaSuccess) return noalloc_fail(HS_ERR_CUDA, cudaGetErrorString(e));
@@ -103,9 +103,12 @@ extern "C" int hs_resolve_noalloc(hs_stream_t stream, int num_requests, int cont
     hs::carve_miss_area(L, base);
     L.status = status ? status : reinterpret_cast<uint32_t*>(base + area);
     cudaStream_t s = (cudaStream_t)stream;
-    if ((e = hs::launch_resolve(L, s, selections, k, out_slots, miss_counts, true)) != cudaSuccess)
+    if ((e = hs::launch_resolve(L, s, selections, k, out_slots, miss_counts)) != cudaSuccess)
         return noalloc_fail(HS_ERR_CUDA, cudaGetErrorString(e));
-    if ((e = hs::launch_gather(L, s, d->num_sms, hs::overlap_fetch(R, d->num_sms))) != cudaSuccess)
+    // Callers with different state buffers share this array, and a flag left by one of
+    // them could carry another's tag: the fetch therefore runs after the resolution
+    // here (no overlap), when every flag it reads has been written by this call.
+    if ((e = hs::launch_gather(L, s, d->num_sms, false)) != cudaSuccess)
         return noalloc_fail(HS_ERR_CUDA, cudaGetErrorString(e));
     hs::record_error("");
     return HS_OK;

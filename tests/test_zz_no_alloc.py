@@ -82,3 +82,42 @@ def test_noalloc_matches_resolve_call_after_call():
     torch.cuda.synchronize()
     assert torch.equal(ref.step(), st["step"])
     ref.close()
+
+
+def test_noalloc_callers_with_separate_state_can_alternate():
+    """Two callers (say two layers) each own their state and take turns; the library's
+    shared scratch must not leak one caller's hand-off into the other's call."""
+    hs.build()
+    tracegen.build()
+    lib = hs.load_library()
+    w = tracegen.WORKLOADS["dsa"]
+    B, T = 4, 6
+    refs = [hs.Context(B, w.C, w.S, w.E) for _ in range(2)]
+    for layer, ref in enumerate(refs):
+        tracegen.fill_kv(ref.host_kv_address(), ref.host_stride, w, B=B, layer=layer)
+    states = [{
+        "pt": torch.full((B, w.C), -1, dtype=torch.int32, device="cuda"),
+        "tok": torch.full((B, w.S), -1, dtype=torch.int32, device="cuda"),
+        "lu": torch.full((B, w.S), -1, dtype=torch.int32, device="cuda"),
+        "step": torch.zeros(B, dtype=torch.int32, device="cuda"),
+        "dev": torch.zeros((B, w.S, w.E), dtype=torch.uint8, device="cuda"),
+    } for _ in range(2)]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sel = torch.from_numpy(tracegen.trace(w, T=T, B=B)).cuda()
+    wb = tracegen.Workload("dsa4", w.config, B=B, L=1, C=w.C, S=w.S, k=w.k, E=w.E, kv_kind=w.kv_kind,
+                           T=T, keep_pct=w.keep_pct, zipf_s=w.zipf_s)
+    for t in range(T):
+        for layer in range(2):  # same step count, same selection: tags coincide on purpose
+            a_out, b_out = torch.empty_like(sel[t]), torch.empty_like(sel[t])
+            a_miss = torch.empty(B, dtype=torch.int32, device="cuda")
+            b_miss = torch.empty(B, dtype=torch.int32, device="cuda")
+            refs[layer].resolve(sel[t], a_out, a_miss)
+            rc = _noalloc(lib, wb, refs[layer].host_kv_address(), refs[layer].host_stride, states[layer],
+                          sel[t], b_out, b_miss, status)
+            assert rc == hs.HS_OK, hs.last_error()
+            torch.cuda.synchronize()
+            assert torch.equal(a_out, b_out) and torch.equal(a_miss, b_miss), (t, layer)
+            assert torch.equal(refs[layer].device_kv(), states[layer]["dev"]), (t, layer)
+    assert int(status.item()) == 0
+    for ref in refs:
+        ref.close()
