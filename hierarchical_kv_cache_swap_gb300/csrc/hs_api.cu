@@ -13,7 +13,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-#include "../../include/hs.h"
+#include "hs.h"
 #include "hs_internal.h"
 
 struct hs_ctx {

@@ -22,6 +22,10 @@ constexpr int kMaxSlots = 65535;                   // slot ids are kept as uint1
 constexpr int kMaxRequests = 1 << 20;        // requests per context
 constexpr uint32_t kSpinLimit = 1u << 21;          // bounded waits on a request's flags
 constexpr int32_t kStepLimit = INT32_MAX - 1;      // calls per request (then refused)
+#ifndef HS_POLL_SLEEP_NS
+#define HS_POLL_SLEEP_NS 64
+#endif
+constexpr unsigned kPollSleepNs = HS_POLL_SLEEP_NS; // pause between polls of a flag
 
 // Everything the two kernels need about one context.
 struct Layout {

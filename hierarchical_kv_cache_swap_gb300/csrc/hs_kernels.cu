@@ -104,7 +104,7 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t want, u
                 atomicOr(status, HS_STATUS_TIMEOUT);
                 break;
             }
-            __nanosleep(64);
+            __nanosleep(kPollSleepNs);
         }
         bcast[0] = ok;
         bcast[1] = v;

@@ -14,7 +14,7 @@
 
 #include <mutex>
 
-#include "../../include/hs.h"
+#include "hs.h"
 #include "hs_internal.h"
 
 namespace {

@@ -279,3 +279,41 @@ def test_contexts_of_different_sizes_coexist():
     b.close()
     run_and_compare(big, T=6, B=2)
     run_and_compare(small, T=6)
+
+
+def test_no_copy_calls_interleaved_with_fetching_calls():
+    """A call without the fetch (HS_FLAG_NO_COPY) between fetching calls leaves a hand-off
+    the next fetch must not mistake for its own: tables, outputs and the rows fetched by
+    fetching calls must still match the oracle."""
+    w = tracegen.WORKLOADS["dsa"]
+    B, T = 4, 24
+    run = GpuRun(w, T, B=B)
+    o = Oracle(B, w.C, w.S, w.E)
+    base = run.ctx.host_kv_address()
+    row_bytes = w.C * run.ctx.host_stride
+    fetched = [set() for _ in range(B)]  # slots (re)filled by a fetching call
+    for t in range(T):
+        no_copy = t % 3 == 1
+        run.ctx.set_flags(hs.HS_FLAG_NO_COPY if no_copy else 0)
+        run.step(t)
+        torch.cuda.synchronize()
+        out = run.out_dev[t].cpu().numpy()
+        miss = run.miss_dev[t].cpu().numpy()
+        tok_before = o.tok.copy()
+        for b in range(B):
+            o_out, o_m, _ = o.resolve_request(b, base + b * row_bytes, run.ctx.host_stride, run.sel[t, b])
+            assert np.array_equal(o_out, out[b]) and o_m == miss[b], (t, b)
+            changed = set(np.nonzero(o.tok[b] != tok_before[b])[0].tolist())
+            if no_copy:
+                fetched[b] -= changed
+            else:
+                fetched[b] |= changed
+    for name, ref in (("page_table", o.pt), ("slot_token", o.tok), ("last_use", o.lu), ("step", o.t)):
+        assert np.array_equal(getattr(run.ctx, name)().cpu().numpy(), ref), name
+    dev = run.ctx.device_kv().cpu().numpy()
+    for b in range(B):
+        rows = sorted(fetched[b])
+        assert rows, b
+        assert np.array_equal(dev[b, rows], o.dev_rows(b)[rows]), b
+    assert run.ctx.status() == 0
+    run.close()
