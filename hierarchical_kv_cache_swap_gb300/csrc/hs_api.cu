@@ -79,7 +79,7 @@ int enqueue(hs_ctx* h, cudaStream_t s, const int32_t* sel, int k, int32_t* out, 
     const bool fetch = !(h->flags & HS_FLAG_NO_COPY);
     cudaError_t e;
     if (ev && (e = cudaEventRecord(ev[0], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    if ((e = hs::launch_resolve(h->L, s, sel, k, out, miss)) != cudaSuccess)
+    if ((e = hs::launch_resolve(h->L, s, sel, k, out, miss, fetch)) != cudaSuccess)
         return cuda_fail(e, "resolution kernel launch");
     if (ev && (e = cudaEventRecord(ev[1], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     // chained by programmatic dependent launch unless events sit between the kernels
@@ -194,7 +194,7 @@ hs_ctx* create(int num_requests, int context_len, int slots, int entry_bytes, ui
     HS_ALLOC(L.tok, sizeof(int32_t) * (size_t)R * S);
     HS_ALLOC(L.lu, sizeof(int32_t) * (size_t)R * S);
     HS_ALLOC(L.step, sizeof(int32_t) * (size_t)R);
-    HS_ALLOC(h->miss_area, hs::miss_area_bytes(R, S));
+    HS_ALLOC(h->miss_area, hs::miss_area_bytes(R, S, sms));
     hs::carve_miss_area(L, h->miss_area);
     HS_ALLOC(L.status, sizeof(uint32_t));
     HS_ALLOC(h->stage_sel, sizeof(int32_t) * (size_t)R * S);
@@ -266,7 +266,7 @@ int hs_reset(hs_ctx* h, hs_stream_t stream) {
         (e = cudaMemsetAsync(L.tok, 0xff, sizeof(int32_t) * (size_t)L.R * L.S, s)) != cudaSuccess ||
         (e = cudaMemsetAsync(L.lu, 0xff, sizeof(int32_t) * (size_t)L.R * L.S, s)) != cudaSuccess ||
         (e = cudaMemsetAsync(L.step, 0, sizeof(int32_t) * (size_t)L.R, s)) != cudaSuccess ||
-        (e = cudaMemsetAsync(h->miss_area, 0, hs::miss_area_bytes(L.R, L.S), s)) != cudaSuccess ||
+        (e = cudaMemsetAsync(h->miss_area, 0, hs::miss_area_bytes(L.R, L.S, h->num_sms), s)) != cudaSuccess ||
         (e = cudaMemsetAsync(L.status, 0, sizeof(uint32_t), s)) != cudaSuccess ||
         (e = cudaMemsetAsync(L.dev, 0, (size_t)L.R * L.S * L.E, s)) != cudaSuccess)
         return cuda_fail(e, "cudaMemsetAsync");

@@ -21,11 +21,8 @@ constexpr int kGatherUnroll = 8;                   // 16-byte loads in flight pe
 constexpr int kMaxSlots = 65535;                   // slot ids are kept as uint16 in shared memory
 constexpr int kMaxRequests = 1 << 20;        // requests per context
 constexpr uint32_t kSpinLimit = 1u << 21;          // bounded waits on a request's flags
-constexpr int32_t kStepLimit = INT32_MAX - 1;      // calls per request (then refused)
-#ifndef HS_POLL_SLEEP_NS
-#define HS_POLL_SLEEP_NS 64
-#endif
-constexpr unsigned kPollSleepNs = HS_POLL_SLEEP_NS; // pause between polls of a flag
+constexpr unsigned kPollSleepNs = 32;              // first pause between polls of a flag,
+constexpr unsigned kPollSleepMaxNs = 256;          // doubling up to this (fewer polls, less L2 traffic)
 
 // Everything the two kernels need about one context.
 struct Layout {
@@ -41,13 +38,14 @@ struct Layout {
     // miss area, shared by the two kernels of a call (carve_miss_area):
     int32_t* mpos;         // [R][S]: position of the r-th miss (ascending)
     int32_t* mslot;        // [R][S]: slot the r-th miss takes
-    uint32_t* ready_pos;   // [R]: (step_b mod 2^16) << 16 | m_b once mpos of request b is published
-    uint32_t* ready_slot;  // [R]: == step_b once mslot of request b is published
+    uint32_t* ready_pos;   // [R]: (tag mod 2^16) << 16 | m_b once mpos of request b is published
+    uint32_t* ready_slot;  // [R]: == tag once mslot of request b is published
+    uint32_t* gcount;      // [R + G]: fetch CTA counters; (b, share q) at b + q*R; tag = gcount[b] + 1
 };
 
 // Bytes of the miss area for R requests of S slots, and its layout at `base`
 // (16-byte aligned). An all-zero area is a valid initial state.
-size_t miss_area_bytes(int R, int S);
+size_t miss_area_bytes(int R, int S, int num_sms);
 void carve_miss_area(Layout& L, void* base);
 
 // Dynamic shared memory of one request's resolution for (C, S).
@@ -58,15 +56,16 @@ size_t gather_smem_bytes();
 // device must be `device`); returns a CUDA error.
 cudaError_t configure_kernels(int device);
 
-// Enqueue the resolution kernel (one CTA per request). It publishes each request's
-// miss positions as soon as they are ranked and the victim slots once chosen.
+// Enqueue the resolution kernel (one CTA per request). With `fetch` (a fetch grid is
+// enqueued next) it publishes each request's miss positions as soon as they are ranked
+// and the victim slots once chosen.
 cudaError_t launch_resolve(const Layout& L, cudaStream_t stream, const int32_t* sel, int k,
-                           int32_t* out_slots, int32_t* miss_counts);
+                           int32_t* out_slots, int32_t* miss_counts, bool fetch);
 
 // Enqueue the row fetch (a persistent grid of kGatherCtasPerSm CTAs per SM). With
 // `pdl` it is chained to the preceding resolution by programmatic dependent launch and
 // runs concurrently with it, starting on each request's rows as soon as they are
-// published; without it, it runs after the resolution.
+// published; without it, it runs after the resolution and reads the hand-off as is.
 // Overlap pays when the resolution leaves SMs free for the fetch grid.
 inline bool overlap_fetch(int R, int num_sms) { return R <= num_sms; }
 cudaError_t launch_gather(const Layout& L, cudaStream_t stream, int num_sms, bool pdl);

@@ -27,11 +27,12 @@
 //   into their HBM slots. The host-link transfer -- the only real cost of the step --
 //   thus overlaps the victim ranking and the table updates, and uses every SM's load
 //   slots, not just the CTAs of the requests.
-// Flags are tagged with the request's step after the call: the resolution advances
-// step[b] and makes it visible before it lets the fetch grid launch, so a fetch CTA
-// reads its call's tag from step[b]; every call publishes both flags, so a flag left
-// from the previous call never carries the current tag, and graph replays need no host
-// reset. Every wait is bounded: on expiry
+// Flags carry a per-request call tag: each fetch CTA keeps a private counter for each
+// (request, share) it serves and advances it once per call; the resolution reads share
+// 0's counter of its request and tags the call's flags with counter + 1. A flag left
+// from an earlier call never carries the tag a later fetch waits for (calls without a
+// fetch publish nothing and advance nothing), and graph replays need no host reset.
+// Every wait is bounded: on expiry
 // the CTA records HS_STATUS_TIMEOUT and skips, so no wait can hang the GPU.
 //
 // No tensor cores: nothing here is a contraction.
@@ -85,8 +86,9 @@ __device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
 
 // All threads' global writes so far become visible before *flag = value: the barrier
 // orders them before thread 0's release store, which is cumulative. Called by every
-// thread of the CTA.
-__device__ __forceinline__ void publish(uint32_t* flag, uint32_t value) {
+// thread of the CTA; a no-op when `on` is false.
+__device__ __forceinline__ void publish(uint32_t* flag, uint32_t value, bool on) {
+    if (!on) return;
     __syncthreads();
     if (threadIdx.x == 0) st_release(flag, value);
 }
@@ -104,7 +106,7 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t want, u
                 atomicOr(status, HS_STATUS_TIMEOUT);
                 break;
             }
-            __nanosleep(kPollSleepNs);
+            __nanosleep(min(kPollSleepNs << min(it, 4u), kPollSleepMaxNs));  // backing off
         }
         bcast[0] = ok;
         bcast[1] = v;
@@ -193,7 +195,7 @@ struct Request {
     uint16_t* sa;
     uint16_t* sb;
     uint32_t m = 0, N = 0, miss_base = 0, cand_base = 0;
-    int g0 = 0, g1 = 0, w0 = 0, w1 = 0;
+    int g0 = 0, g1 = 0, s0 = 0, s1 = 0;  // this thread's miss-bitmap groups and slot range
     const uint16_t* victims = nullptr;  // victims[r] = slot of the r-th miss
 
     __device__ Request(const Layout& L_, const Plan& P_, uint8_t* smem_, const int32_t* sel, int k_,
@@ -229,10 +231,17 @@ struct Request {
         asm volatile("cp.async.commit_group;" ::: "memory");
         for (int i = tid; i < P.CW; i += NT) posbm[i] = 0u;
         for (int i = tid; i < P.SW; i += NT) hitbm[i] = 0u;
+        if (tid == 0) {
+            scratch[2 * NW] = 0xffffffffu;  // running min / max of the candidates' keys
+            scratch[2 * NW + 1] = 0u;
+        }
     }
 
-    // Loads the selections j0 + q*NT + tid (q < 4) and their page-table entries.
-    __device__ __forceinline__ void load_batch(int j0, int32_t (&p)[4], int32_t (&s)[4]) const {
+    // Loads the selections j0 + q*NT + tid (q < 4) and their page-table entries; with
+    // `extra`, also *extra_out = *extra, issued together with the selections.
+    __device__ __forceinline__ void load_batch(int j0, int32_t (&p)[4], int32_t (&s)[4],
+                                               const int32_t* extra = nullptr,
+                                               int32_t* extra_out = nullptr) const {
         const int tid = threadIdx.x;
         const int C = L.C;
 #pragma unroll
@@ -240,6 +249,7 @@ struct Request {
             const int j = j0 + q * NT + tid;
             p[q] = j < k ? __ldg(selb + j) : -1;
         }
+        if (extra) *extra_out = *(volatile const int32_t*)extra;
 #pragma unroll
         for (int q = 0; q < 4; ++q) s[q] = (p[q] >= 0 && p[q] < C) ? ptb[p[q]] : -1;
     }
@@ -262,7 +272,7 @@ struct Request {
         uint32_t st = 0;
         int any_miss = 0;
         for (int j0 = 0; j0 < k; j0 += 4 * NT) {
-            if (j0 > 0) load_batch(j0, p, s);
+            if (j0 > 0) load_batch(j0, p, s);  // only when k > 4 * NT (then answers re-read)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int j = j0 + q * NT + tid;
@@ -289,9 +299,12 @@ struct Request {
 
     __device__ void drain() const { cp_async_wait_all(); }
 
-    __device__ uint32_t word_mask(int w) const {
-        const int S = L.S;
-        return (w == P.SW - 1 && (S & 31)) ? ((1u << (S & 31)) - 1u) : 0xffffffffu;
+    // Non-hit slots among [lo, hi) -- a range inside one bitmap word, or whole words.
+    __device__ __forceinline__ uint32_t cand_bits(int lo, int hi) const {
+        const uint32_t word = ~hitbm[lo >> 5];
+        const int n = hi - lo;
+        const uint32_t mask = n >= 32 ? 0xffffffffu : ((1u << n) - 1u) << (lo & 31);
+        return word & mask;
     }
 
     // 2. miss count and ascending-position ranks; candidate count; mpos[] filled.
@@ -300,14 +313,17 @@ struct Request {
         const int gpt = (P.CG + NT - 1) / NT;
         g0 = min(tid * gpt, P.CG);
         g1 = min(g0 + gpt, P.CG);
-        const int wpt = (P.SW + NT - 1) / NT;
-        w0 = min(tid * wpt, P.SW);
-        w1 = min(w0 + wpt, P.SW);
+        // slots per thread: a power of two, so a thread's range never straddles a word
+        // boundary unless it is made of whole words
+        int spt = 1;
+        while (spt * NT < L.S) spt <<= 1;
+        s0 = min(tid * spt, L.S);
+        s1 = min(s0 + spt, L.S);
         uint32_t nmiss = 0, ncand = 0;
         for (int g = g0; g < g1; ++g)
 #pragma unroll
             for (int q = 0; q < kGroupWords; ++q) nmiss += __popc(posbm[g * kGroupWords + q]);
-        for (int w = w0; w < w1; ++w) ncand += __popc(~hitbm[w] & word_mask(w));
+        for (int lo = s0; lo < s1; lo = min((lo | 31) + 1, s1)) ncand += __popc(cand_bits(lo, min((lo | 31) + 1, s1)));
         uint32_t total;
         const uint32_t excl = block_exclusive_scan<NT>((ncand << 16) | nmiss, scratch, &total);
         m = total & 0xffffu;
@@ -337,10 +353,10 @@ struct Request {
         uint32_t kmin = 0xffffffffu, kmax = 0u;
         {
             uint32_t c = cand_base;
-            for (int w = w0; w < w1; ++w) {
-                uint32_t bits = ~hitbm[w] & word_mask(w);
+            for (int lo = s0; lo < s1; lo = min((lo | 31) + 1, s1)) {
+                uint32_t bits = cand_bits(lo, min((lo | 31) + 1, s1));
                 while (bits) {
-                    const int s = w * 32 + __ffs(bits) - 1;
+                    const int s = (lo & ~31) + __ffs(bits) - 1;
                     bits &= bits - 1;
                     sa[c++] = (uint16_t)s;
                     const uint32_t key = keys[s] + 1u;
@@ -351,38 +367,28 @@ struct Request {
         }
         kmin = __reduce_min_sync(0xffffffffu, kmin);
         kmax = __reduce_max_sync(0xffffffffu, kmax);
+        uint32_t* kr = scratch + 2 * NW;  // [min, max], initialised in start()
         if (lane == 0) {
-            scratch[warp] = kmin;
-            scratch[NW + warp] = kmax;
+            atomicMin(kr, kmin);
+            atomicMax(kr + 1, kmax);
         }
         __syncthreads();
-        if (tid == 0) {
-            uint32_t a = scratch[0], z = scratch[NW];
-            for (int i = 1; i < NW; ++i) {
-                a = min(a, scratch[i]);
-                z = max(z, scratch[NW + i]);
-            }
-            scratch[2 * NW] = a;
-            scratch[2 * NW + 1] = z;
-        }
-        __syncthreads();
-        kmin = scratch[2 * NW];
-        kmax = scratch[2 * NW + 1];
-        __syncthreads();  // scratch is reused by the scans below
+        kmin = kr[0];
+        kmax = kr[1];
 
         const uint32_t range = kmax - kmin;
         const int npass = range ? (32 - __clz(range) + kRadixBits - 1) / kRadixBits : 0;
         const int seg = (((int)N + NW - 1) / NW + 31) & ~31;
-        const int s0 = min(warp * seg, (int)N), s1 = min(s0 + seg, (int)N);
+        const int e0 = min(warp * seg, (int)N), e1 = min(e0 + seg, (int)N);
         uint16_t* src = sa;
         uint16_t* dst = sb;
         for (int pass = 0; pass < npass; ++pass) {
             const int shift = pass * kRadixBits;
             for (int i = tid; i < kBins * NW / 2; i += NT) reinterpret_cast<uint32_t*>(counts)[i] = 0u;
             __syncthreads();
-            for (int base = s0; base < s1; base += 32) {
+            for (int base = e0; base < e1; base += 32) {
                 const int idx = base + lane;
-                const bool v = idx < s1;
+                const bool v = idx < e1;
                 const uint32_t d = v ? ((keys[src[idx]] + 1u - kmin) >> shift) & (kBins - 1) : (uint32_t)kBins;
                 const uint32_t peers = __match_any_sync(0xffffffffu, d);
                 if (v && lane == __ffs(peers) - 1) counts[d * NW + warp] += (uint16_t)__popc(peers);
@@ -406,9 +412,9 @@ struct Request {
                 }
             }
             __syncthreads();
-            for (int base = s0; base < s1; base += 32) {
+            for (int base = e0; base < e1; base += 32) {
                 const int idx = base + lane;
-                const bool v = idx < s1;
+                const bool v = idx < e1;
                 const uint16_t sl = v ? src[idx] : (uint16_t)0;
                 const uint32_t d = v ? ((keys[sl] + 1u - kmin) >> shift) & (kBins - 1) : (uint32_t)kBins;
                 const uint32_t peers = __match_any_sync(0xffffffffu, d);
@@ -447,61 +453,65 @@ struct Request {
     }
 
     // 4c. answers for the missed selections (their rank through the bitmap).
-    __device__ void answer_misses() {
-        const int C = L.C;
-        for (int j = threadIdx.x; j < k; j += NT) {
-            const int32_t p = __ldg(selb + j);
-            if (p < 0 || p >= C) continue;
-            const int w = p >> 5;
-            const uint32_t bit = 1u << (p & 31);
-            const uint32_t word = posbm[w];
-            if (!(word & bit)) continue;  // a hit, already answered
-            const int g = w / kGroupWords;
-            uint32_t rank = gprefix[g];
-            for (int q = g * kGroupWords; q < w; ++q) rank += __popc(posbm[q]);
-            rank += __popc(word & (bit - 1u));
-            outb[j] = victims[rank];
+    __device__ __forceinline__ void answer(int j, int32_t p) {
+        if (p < 0 || p >= L.C) return;
+        const int w = p >> 5;
+        const uint32_t bit = 1u << (p & 31);
+        const uint32_t word = posbm[w];
+        if (!(word & bit)) return;  // a hit, already answered
+        const int g = w / kGroupWords;
+        uint32_t rank = gprefix[g];
+        for (int q = g * kGroupWords; q < w; ++q) rank += __popc(posbm[q]);
+        rank += __popc(word & (bit - 1u));
+        outb[j] = victims[rank];
+    }
+
+    // p: the selections this thread probed in the first batch (still in registers).
+    __device__ void answer_misses(const int32_t (&p)[4]) {
+        if (k <= 4 * NT) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = q * NT + threadIdx.x;
+                if (j < k) answer(j, p[q]);
+            }
+        } else {
+            for (int j = threadIdx.x; j < k; j += NT) answer(j, __ldg(selb + j));
         }
     }
 
     __device__ void finish(int32_t* miss_counts, uint32_t misses) {
-        if (threadIdx.x == 0) miss_counts[b] = (int32_t)misses;
+        if (threadIdx.x == 0) {
+            miss_counts[b] = (int32_t)misses;
+            L.step[b] = t + 1;
+        }
     }
 };
 
 __global__ void __launch_bounds__(kResolveThreads, 2)
 resolve_kernel(const Layout L, const int32_t* __restrict__ sel, int k, int32_t* __restrict__ out,
-               int32_t* __restrict__ miss_counts) {
+               int32_t* __restrict__ miss_counts, int fetch) {
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ int32_t t_sh;
+    pdl_launch_dependents();  // the fetch grid may start now; it synchronizes per request
     const int b = blockIdx.x;
     const Plan P(L.C, L.S);
     Request R(L, P, smem, sel, k, out);
-    // Thread 0 advances the request's step and makes it visible GPU-wide before it lets
-    // the fetch grid launch: the new step is this call's tag on both flags (a request
-    // at its call limit keeps the saturated step and publishes "no misses"). Meanwhile
-    // the other threads start on the selections and the page table.
-    if (threadIdx.x == 0) {
-        const int32_t t0 = L.step[b];
-        L.step[b] = t0 < kStepLimit ? t0 + 1 : INT32_MAX;
-        __threadfence();
-        pdl_launch_dependents();  // the fetch grid may start; it synchronizes per request
-        t_sh = t0;
-    }
-    R.start();
     int32_t p[4], s[4];
     R.load_batch(0, p, s);
-    __syncthreads();  // bitmaps cleared, t_sh set
-    const int32_t t0 = t_sh;
-    const uint32_t ready = (uint32_t)(t0 < kStepLimit ? t0 + 1 : INT32_MAX);
+    // the call's stamp and tag (read once by every thread; both only change between calls)
+    const int32_t t0 = *(volatile const int32_t*)(L.step + b);
+    const uint32_t ready = ld_relaxed(L.gcount + b) + 1u;
+    // Flags are raised only when a fetch grid follows (it advances the counters).
+    const bool pub = fetch != 0;
     // ready_pos carries the tag's low half in its high half and the miss count in its
     // low half, so a fetch CTA learns both from the one acquire load it waits on.
     const uint32_t tag = (ready & 0xffffu) << 16;
     uint32_t* rpos = L.ready_pos + b;
     uint32_t* rslot = L.ready_slot + b;
-    if (t0 >= kStepLimit) {  // refused: nothing to fetch for this request
+    R.start();
+    __syncthreads();  // bitmaps cleared
+    if (t0 == INT32_MAX) {  // refused: the request reached its call limit
         R.refuse(miss_counts);
-        if (threadIdx.x == 0) {
+        if (pub && threadIdx.x == 0) {
             st_release(rpos, tag);
             st_release(rslot, ready);
         }
@@ -509,7 +519,7 @@ resolve_kernel(const Layout L, const int32_t* __restrict__ sel, int k, int32_t* 
     }
     R.t = t0;
     if (!R.probe(p, s)) {  // all hits: nothing to rank or fetch
-        if (threadIdx.x == 0) {
+        if (pub && threadIdx.x == 0) {
             st_release(rpos, tag);
             st_release(rslot, ready);
         }
@@ -519,20 +529,24 @@ resolve_kernel(const Layout L, const int32_t* __restrict__ sel, int k, int32_t* 
     }
     R.rank_misses();
     R.export_misses();
-    publish(rpos, tag | R.m);  // the fetch of this request's rows can start
+    publish(rpos, tag | R.m, pub);  // the fetch of this request's rows can start
     R.rank_victims();
     R.apply();
-    publish(rslot, ready);  // ... and its rows can be stored
-    R.answer_misses();
+    publish(rslot, ready, pub);  // ... and its rows can be stored
+    R.answer_misses(p);
     R.finish(miss_counts, R.m);
 }
 
 // One fetch CTA's share of request b: rows q, q + nq, q + 2nq, ... of its m misses.
 __device__ __forceinline__ void fetch_rows(const Layout& L, int b, uint32_t q, uint32_t nq, uint32_t ready,
-                                           uint32_t* bcast) {
+                                           bool sync, uint32_t* bcast) {
     constexpr int GT = kGatherThreads;
     uint32_t v;
-    if (!wait_flag(L.ready_pos + b, (ready & 0xffffu) << 16, 0xffff0000u, L.status, bcast, &v)) return;
+    if (sync) {
+        if (!wait_flag(L.ready_pos + b, (ready & 0xffffu) << 16, 0xffff0000u, L.status, bcast, &v)) return;
+    } else {  // launched after the resolution: its hand-off is complete
+        v = ld_relaxed(L.ready_pos + b);
+    }
     const uint32_t m = v & 0xffffu;
     const uint32_t cpr = (uint32_t)L.E >> 4;
     const uint32_t rows = m > q ? (m - q + nq - 1) / nq : 0u;
@@ -554,7 +568,7 @@ __device__ __forceinline__ void fetch_rows(const Layout& L, int b, uint32_t q, u
             }
         }
         if (!slots_known) {  // the loads above are in flight while the victims are ranked
-            if (!wait_flag(L.ready_slot + b, ready, 0xffffffffu, L.status, bcast, &v)) return;
+            if (sync && !wait_flag(L.ready_slot + b, ready, 0xffffffffu, L.status, bcast, &v)) return;
             slots_known = true;
         }
 #pragma unroll
@@ -569,21 +583,26 @@ __device__ __forceinline__ void fetch_rows(const Layout& L, int b, uint32_t q, u
     }
 }
 
-// Request b's fetch by nq CTAs (this one is share q), for the call tagged step[b].
-__device__ __forceinline__ void fetch_request(const Layout& L, int b, uint32_t q, uint32_t nq, uint32_t* bcast) {
-    const uint32_t ready = ld_relaxed(reinterpret_cast<const uint32_t*>(L.step + b));
-    fetch_rows(L, b, q, nq, ready, bcast);
+// Request b's fetch by nq CTAs (this one is share q). The CTA's own counter for
+// (b, q) gives the call's tag and advances once the share is done.
+__device__ __forceinline__ void fetch_request(const Layout& L, int b, uint32_t q, uint32_t nq, bool sync,
+                                              uint32_t* bcast) {
+    uint32_t* count = L.gcount + b + (size_t)q * L.R;
+    const uint32_t ready = ld_relaxed(count) + 1u;
+    fetch_rows(L, b, q, nq, ready, sync, bcast);
+    __syncthreads();
+    if (threadIdx.x == 0) *count = ready;
 }
 
 __global__ void __launch_bounds__(kGatherThreads, kGatherCtasPerSm)
-gather_kernel(const Layout L) {
+gather_kernel(const Layout L, int sync) {
     __shared__ uint32_t bcast[2];
     const uint32_t G = gridDim.x, c = blockIdx.x, R = (uint32_t)L.R;
     if (G >= R) {  // several CTAs share each request
         const uint32_t b = c % R;
-        fetch_request(L, (int)b, c / R, (G - 1 - b) / R + 1, bcast);
+        fetch_request(L, (int)b, c / R, (G - 1 - b) / R + 1, sync != 0, bcast);
     } else {  // each CTA takes whole requests
-        for (uint32_t b = c; b < R; b += G) fetch_request(L, (int)b, 0, 1, bcast);
+        for (uint32_t b = c; b < R; b += G) fetch_request(L, (int)b, 0, 1, sync != 0, bcast);
     }
 }
 
@@ -593,10 +612,11 @@ size_t resolve_smem_bytes(int C, int S) { return Plan(C, S).fixed; }
 
 size_t gather_smem_bytes() { return 0; }
 
-size_t miss_area_bytes(int R, int S) {
+size_t miss_area_bytes(int R, int S, int num_sms) {
     const size_t list = ((size_t)R * S * 4 + 15) & ~(size_t)15;
     const size_t per = ((size_t)R * 4 + 15) & ~(size_t)15;
-    return 2 * list + 2 * per;
+    const size_t counters = (size_t)R + (size_t)num_sms * kGatherCtasPerSm;  // >= R * ceil(G / R)
+    return 2 * list + 2 * per + counters * 4;
 }
 
 void carve_miss_area(Layout& L, void* base) {
@@ -608,6 +628,7 @@ void carve_miss_area(Layout& L, void* base) {
     p += 2 * list;
     L.ready_pos = reinterpret_cast<uint32_t*>(p);
     L.ready_slot = reinterpret_cast<uint32_t*>(p + per);
+    L.gcount = reinterpret_cast<uint32_t*>(p + 2 * per);
 }
 
 cudaError_t configure_kernels(int device) {
@@ -623,9 +644,9 @@ cudaError_t configure_kernels(int device) {
 }
 
 cudaError_t launch_resolve(const Layout& L, cudaStream_t stream, const int32_t* sel, int k,
-                           int32_t* out_slots, int32_t* miss_counts) {
+                           int32_t* out_slots, int32_t* miss_counts, bool fetch) {
     resolve_kernel<<<L.R, kResolveThreads, resolve_smem_bytes(L.C, L.S), stream>>>(L, sel, k, out_slots,
-                                                                                   miss_counts);
+                                                                                   miss_counts, fetch ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -640,7 +661,7 @@ cudaError_t launch_gather(const Layout& L, cudaStream_t stream, int num_sms, boo
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gather_kernel, L);
+    return cudaLaunchKernelEx(&cfg, gather_kernel, L, pdl ? 1 : 0);
 }
 
 }  // namespace hs

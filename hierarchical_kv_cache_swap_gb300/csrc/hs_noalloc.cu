@@ -74,11 +74,18 @@ extern "C" int hs_resolve_noalloc(hs_stream_t stream, int num_requests, int cont
         return noalloc_fail(HS_ERR_LIMIT, "slots or num_requests beyond this build's limits");
     if ((unsigned long long)R * S * (E / 16) > (1ull << 31))
         return noalloc_fail(HS_ERR_LIMIT, "device buffer beyond 32 GiB");
-    const size_t area = hs::miss_area_bytes(R, S);
+    int nsm = 0;
+    {
+        int dv = -1;
+        cudaError_t e0 = cudaGetDevice(&dv);
+        if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dv);
+        if (e0 != cudaSuccess) return noalloc_fail(HS_ERR_CUDA, cudaGetErrorString(e0));
+    }
+    const size_t area = hs::miss_area_bytes(R, S, nsm);
     if (area + sizeof(uint32_t) > HS_NOALLOC_SCRATCH_BYTES)
         return noalloc_fail(HS_ERR_LIMIT,
                             "num_requests * slots too large for the fixed scratch array "
-                            "(about 8*R*S + 8*R bytes must fit in HS_NOALLOC_SCRATCH_BYTES)");
+                            "(about 8*R*S + 12*R + 4*SMs bytes must fit in HS_NOALLOC_SCRATCH_BYTES)");
     int dev = -1, optin = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return noalloc_fail(HS_ERR_CUDA, cudaGetErrorString(e));
@@ -103,11 +110,11 @@ extern "C" int hs_resolve_noalloc(hs_stream_t stream, int num_requests, int cont
     hs::carve_miss_area(L, base);
     L.status = status ? status : reinterpret_cast<uint32_t*>(base + area);
     cudaStream_t s = (cudaStream_t)stream;
-    if ((e = hs::launch_resolve(L, s, selections, k, out_slots, miss_counts)) != cudaSuccess)
+    if ((e = hs::launch_resolve(L, s, selections, k, out_slots, miss_counts, true)) != cudaSuccess)
         return noalloc_fail(HS_ERR_CUDA, cudaGetErrorString(e));
-    // Callers with different state buffers share this array, and a flag left by one of
-    // them could carry another's tag: the fetch therefore runs after the resolution
-    // here (no overlap), when every flag it reads has been written by this call.
+    // Callers with different sizes share this array, so the fetch CTAs' call counters
+    // need not line up with a caller's requests: the fetch therefore runs after the
+    // resolution here (no overlap) and reads the hand-off without waiting on flags.
     if ((e = hs::launch_gather(L, s, d->num_sms, false)) != cudaSuccess)
         return noalloc_fail(HS_ERR_CUDA, cudaGetErrorString(e));
     hs::record_error("");

@@ -63,7 +63,7 @@ typedef struct CUevent_st* hs_event_t;
 /* device status bits (hs_get_status) */
 #define HS_STATUS_RANGE 1u    /* a selection was >= context_len */
 #define HS_STATUS_DUP 2u      /* a position appeared twice in one request's row */
-#define HS_STATUS_STEP_LIMIT 4u /* a request reached 2^31-2 calls; the call was skipped */
+#define HS_STATUS_STEP_LIMIT 4u /* a request reached 2^31-1 calls; the call was skipped */
 #define HS_STATUS_TIMEOUT 8u    /* a fetch waited too long for its resolution (should not happen) */
 
 /* flags (hs_set_flags) */
@@ -210,13 +210,13 @@ const char* hs_last_error(void);
  * the other (hs_resolve overlaps them). The miss list the two kernels
  * share lives in a fixed file-scope device array of HS_NOALLOC_SCRATCH_BYTES bytes,
  * which every GPU that loads this library keeps until the process exits; a call needs
- * about 8*R*S + 8*R bytes of it (up to 64 more for alignment) and larger sizes fail with
+ * about 8*R*S + 12*R + 4*G bytes of it, G = twice the GPU's SM count (up to 64 more
+ * for alignment) and larger sizes fail with
  * HS_ERR_LIMIT before anything is enqueued. Every call on a device shares that device's copy of the array, so calls
  * whose work overlaps on the GPU (on two streams, say) race: serialise them. The array
  * keeps the last call's contents, which the next call continues from: besides the
- * lists every call rewrites, it holds per-request flags that the two kernels use to
- * find each other's results, tagged with the step counters the caller owns; it starts
- * zeroed at load, which is a valid state, and needs no clearing between calls. The first call on a
+ * lists every call rewrites, it holds per-request flags and counters; it starts zeroed at
+ * load, which is a valid state, and needs no clearing between calls. The first call on a
  * device does a one-time set-up with that device current (it looks up the array's
  * device address and sets kernel attributes): make that first call before any stream
  * capture. Returns HS_OK or HS_ERR_* (hs_last_error() describes it).
