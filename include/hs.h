@@ -210,8 +210,8 @@ const char* hs_last_error(void);
  * the other (hs_resolve overlaps them). The miss list the two kernels
  * share lives in a fixed file-scope device array of HS_NOALLOC_SCRATCH_BYTES bytes,
  * which every GPU that loads this library keeps until the process exits; a call needs
- * about 8*R*S + 12*R + 4*G bytes of it, G = twice the GPU's SM count (up to 64 more
- * for alignment) and larger sizes fail with
+ * about 8*R*S + 12*R + 4*G bytes of it, G = the GPU's SM count (up to 64 more for
+ * alignment) and larger sizes fail with
  * HS_ERR_LIMIT before anything is enqueued. Every call on a device shares that device's copy of the array, so calls
  * whose work overlaps on the GPU (on two streams, say) race: serialise them. The array
  * keeps the last call's contents, which the next call continues from: besides the
