@@ -84,7 +84,7 @@ int enqueue(hs_ctx* h, cudaStream_t s, const int32_t* sel, int k, int32_t* out, 
     if (ev && (e = cudaEventRecord(ev[1], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     // chained by programmatic dependent launch unless events sit between the kernels
     const bool pdl = ev == nullptr && hs::overlap_fetch(h->L.R, h->num_sms);
-    if (fetch && (e = hs::launch_gather(h->L, s, h->num_sms, pdl)) != cudaSuccess)
+    if (fetch && (e = hs::launch_gather(h->L, s, out, k, h->num_sms, pdl)) != cudaSuccess)
         return cuda_fail(e, "fetch kernel launch");
     if (ev && (e = cudaEventRecord(ev[2], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     g_err[0] = 0;

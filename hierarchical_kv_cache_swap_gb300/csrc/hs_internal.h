@@ -36,10 +36,10 @@ struct Layout {
     int32_t* step;         // [R]
     uint32_t* status;      // device status word
     // miss area, shared by the two kernels of a call (carve_miss_area):
-    int32_t* mpos;         // [R][S]: position of the r-th miss (ascending)
-    int32_t* mslot;        // [R][S]: slot the r-th miss takes
-    uint32_t* ready_pos;   // [R]: (tag mod 2^16) << 16 | m_b once mpos of request b is published
-    uint32_t* ready_slot;  // [R]: == tag once mslot of request b is published
+    int32_t* fpos;         // [R][S]: fetch list -- positions of the missed selections
+    int32_t* fsel;         // [R][S]: ... and their indices j in the row (list order is arbitrary)
+    uint32_t* ready_pos;   // [R]: (tag mod 2^16) << 16 | list length, once request b's list is published
+    uint32_t* ready_slot;  // [R]: == tag once request b's answers (out_slots) are written
     uint32_t* gcount;      // [R + G]: fetch CTA counters; (b, share q) at b + q*R; tag = gcount[b] + 1
 };
 
@@ -68,7 +68,8 @@ cudaError_t launch_resolve(const Layout& L, cudaStream_t stream, const int32_t* 
 // published; without it, it runs after the resolution and reads the hand-off as is.
 // Overlap pays when the resolution leaves SMs free for the fetch grid.
 inline bool overlap_fetch(int R, int num_sms) { return R <= num_sms; }
-cudaError_t launch_gather(const Layout& L, cudaStream_t stream, int num_sms, bool pdl);
+cudaError_t launch_gather(const Layout& L, cudaStream_t stream, const int32_t* out_slots, int k, int num_sms,
+                          bool pdl);
 
 // Enqueue the consumer stand-in: sums[b] = sum (mod 2^64) of the 8-byte words of the
 // k rows request b resolved to (slots < 0 skipped); zeroes sums first.

@@ -11,20 +11,22 @@
 // resolve_kernel -- one 512-thread CTA per request:
 //   1. probe the page table for every selected position; hits are stamped and
 //      answered in place, misses are marked in a shared position bitmap;
-//   2. rank the misses by ascending position (a group prefix over the bitmap plus
-//      popcounts), write them to the miss area and PUBLISH them (ready_pos): the
-//      source rows of the fetch are known from here on;
-//   3. rank the non-hit slots by (last_use, slot) with a stable LSD radix sort whose
-//      digits are counted per warp (__match_any_sync ranks equal digits inside a
-//      warp, an exclusive scan over the (digit, warp) table orders the warps), pair
-//      the r-th miss with the r-th victim, update page table / slot tokens / stamps,
-//      and PUBLISH the victim slots (ready_slot); answer the missed selections.
+//   2. the probe lists every missed selection (position, index j in the row) in the
+//      miss area as it finds it; right after the probe's barrier the list is
+//      PUBLISHED (ready_pos): the source rows of the fetch are known from here on;
+//   3. rank the misses by ascending position (a group prefix over the bitmap plus
+//      popcounts), rank the non-hit slots by (last_use, slot) with a stable LSD radix
+//      sort whose digits are counted per warp (__match_any_sync ranks equal digits
+//      inside a warp, an exclusive scan over the (digit, warp) table orders the warps),
+//      pair the r-th miss with the r-th victim and answer the missed selections; the
+//      answers name every row's slot, so they are PUBLISHED (ready_slot) before the
+//      page table, slot tokens and stamps are updated.
 // gather_kernel -- a persistent grid of 2 CTAs per SM, launched right behind the
 //   resolution (PDL) so that it is resident while the resolution runs. Each CTA owns
-//   a share of one request's miss rows: it waits for ready_pos, issues the 16-byte
+//   a share of one request's fetch list: it waits for ready_pos, issues the 16-byte
 //   zero-copy loads of its rows from the mapped host store (coalesced, 8 in flight
-//   per thread), waits for ready_slot only when it has to store, and writes the rows
-//   into their HBM slots. The host-link transfer -- the only real cost of the step --
+//   per thread), waits for ready_slot only when it has to store, and writes each row
+//   into the slot the resolution answered for it. The host-link transfer -- the only real cost of the step --
 //   thus overlaps the victim ranking and the table updates, and uses every SM's load
 //   slots, not just the CTAs of the requests.
 // Flags carry a per-request call tag: each fetch CTA keeps a private counter for each
@@ -185,6 +187,8 @@ struct Request {
     int32_t* ptb;
     int32_t* tokb;
     int32_t* lub;
+    int32_t* fpos;      // fetch list (global): positions of the missed selections ...
+    int32_t* fsel;      // ... and their indices j in the row, in no particular order
     uint32_t* posbm;    // missed positions of this call
     uint32_t* gprefix;  // misses before each group of kGroupWords bitmap words
     uint32_t* hitbm;    // slots hit in this call
@@ -206,6 +210,8 @@ struct Request {
         ptb = L.pt + (size_t)b * L.C;
         tokb = L.tok + (size_t)b * L.S;
         lub = L.lu + (size_t)b * L.S;
+        fpos = L.fpos + (size_t)b * L.S;
+        fsel = L.fsel + (size_t)b * L.S;
         posbm = reinterpret_cast<uint32_t*>(smem + P.posbm);
         gprefix = reinterpret_cast<uint32_t*>(smem + P.gprefix);
         hitbm = reinterpret_cast<uint32_t*>(smem + P.hitbm);
@@ -234,6 +240,7 @@ struct Request {
         if (tid == 0) {
             scratch[2 * NW] = 0xffffffffu;  // running min / max of the candidates' keys
             scratch[2 * NW + 1] = 0u;
+            scratch[2 * NW + 2] = 0u;       // entries of the fetch list
         }
     }
 
@@ -283,10 +290,13 @@ struct Request {
                     if (atomicOr(&hitbm[ss >> 5], bit) & bit) st |= HS_STATUS_DUP;
                     lub[ss] = t;
                     outb[j] = ss;
-                } else if (pp >= 0 && pp < C) {  // miss
+                } else if (pp >= 0 && pp < C) {  // miss: marked, and listed for the fetch
                     const uint32_t bit = 1u << (pp & 31);
                     if (atomicOr(&posbm[pp >> 5], bit) & bit) st |= HS_STATUS_DUP;
                     any_miss = 1;
+                    const uint32_t e = atomicAdd(&scratch[2 * NW + 2], 1u);
+                    fpos[e] = pp;
+                    fsel[e] = j;
                 } else {  // padding, or out of range
                     if (pp >= C) st |= HS_STATUS_RANGE;
                     outb[j] = -1;
@@ -431,15 +441,8 @@ struct Request {
         victims = src;
     }
 
-    // 2b. the ranked misses into the miss area (positions, count).
-    __device__ void export_misses() {
-        int32_t* gpos = L.mpos + (size_t)b * L.S;
-        for (uint32_t r = threadIdx.x; r < m; r += NT) gpos[r] = mpos[r];
-    }
-
-    // 4b. pair, unmap, map, stamp, and export the victim slots.
+    // 4b. pair, unmap, map, stamp.
     __device__ void apply() {
-        int32_t* gslot = L.mslot + (size_t)b * L.S;
         for (uint32_t r = threadIdx.x; r < m; r += NT) {
             const int32_t p = mpos[r];
             const int32_t v = victims[r];
@@ -448,7 +451,6 @@ struct Request {
             ptb[p] = v;
             tokb[v] = p;
             lub[v] = t;
-            gslot[r] = v;
         }
     }
 
@@ -527,19 +529,21 @@ resolve_kernel(const Layout L, const int32_t* __restrict__ sel, int k, int32_t* 
         R.drain();
         return;
     }
+    // The fetch list is complete (the probe ended with a barrier, and the release is
+    // cumulative over it): the fetch of this request's rows can start now.
+    if (pub && threadIdx.x == 0) st_release(rpos, tag | R.scratch[2 * NW + 2]);
     R.rank_misses();
-    R.export_misses();
-    publish(rpos, tag | R.m, pub);  // the fetch of this request's rows can start
     R.rank_victims();
-    R.apply();
-    publish(rslot, ready, pub);  // ... and its rows can be stored
     R.answer_misses(p);
+    publish(rslot, ready, pub);  // the answers name the slots: the rows can be stored
+    R.apply();
     R.finish(miss_counts, R.m);
 }
 
-// One fetch CTA's share of request b: rows q, q + nq, q + 2nq, ... of its m misses.
-__device__ __forceinline__ void fetch_rows(const Layout& L, int b, uint32_t q, uint32_t nq, uint32_t ready,
-                                           bool sync, uint32_t* bcast) {
+// One fetch CTA's share of request b: entries q, q + nq, q + 2nq, ... of its fetch
+// list (position p, selection index j); the row of p goes to slot out[b][j].
+__device__ __forceinline__ void fetch_rows(const Layout& L, const int32_t* out, int k, int b, uint32_t q,
+                                           uint32_t nq, uint32_t ready, bool sync, uint32_t* bcast) {
     constexpr int GT = kGatherThreads;
     uint32_t v;
     if (sync) {
@@ -547,24 +551,25 @@ __device__ __forceinline__ void fetch_rows(const Layout& L, int b, uint32_t q, u
     } else {  // launched after the resolution: its hand-off is complete
         v = ld_relaxed(L.ready_pos + b);
     }
-    const uint32_t m = v & 0xffffu;
+    const uint32_t u = v & 0xffffu;  // entries in the fetch list
     const uint32_t cpr = (uint32_t)L.E >> 4;
-    const uint32_t rows = m > q ? (m - q + nq - 1) / nq : 0u;
+    const uint32_t rows = u > q ? (u - q + nq - 1) / nq : 0u;
     const uint32_t n = rows * cpr;
-    const int32_t* gpos = L.mpos + (size_t)b * L.S;
-    const int32_t* gslot = L.mslot + (size_t)b * L.S;
+    const int32_t* gpos = L.fpos + (size_t)b * L.S;
+    const int32_t* gsel = L.fsel + (size_t)b * L.S;
+    const int32_t* ob = out + (size_t)b * k;
     const uint8_t* hb = L.host + (size_t)b * L.C * L.host_stride;
     uint8_t* db = L.dev + (size_t)b * L.S * L.E;
     bool slots_known = false;
     for (uint32_t base = 0; base < n; base += GT * kGatherUnroll) {
         uint4 val[kGatherUnroll];
 #pragma unroll
-        for (int u = 0; u < kGatherUnroll; ++u) {
-            const uint32_t c = base + (uint32_t)u * GT + threadIdx.x;
+        for (int u8 = 0; u8 < kGatherUnroll; ++u8) {
+            const uint32_t c = base + (uint32_t)u8 * GT + threadIdx.x;
             if (c < n) {
                 const uint32_t lr = c / cpr, off = c - lr * cpr;
                 const int32_t p = __ldcg(gpos + q + nq * lr);
-                val[u] = __ldcs(reinterpret_cast<const uint4*>(hb + (size_t)p * L.host_stride) + off);
+                val[u8] = __ldcs(reinterpret_cast<const uint4*>(hb + (size_t)p * L.host_stride) + off);
             }
         }
         if (!slots_known) {  // the loads above are in flight while the victims are ranked
@@ -572,12 +577,12 @@ __device__ __forceinline__ void fetch_rows(const Layout& L, int b, uint32_t q, u
             slots_known = true;
         }
 #pragma unroll
-        for (int u = 0; u < kGatherUnroll; ++u) {
-            const uint32_t c = base + (uint32_t)u * GT + threadIdx.x;
+        for (int u8 = 0; u8 < kGatherUnroll; ++u8) {
+            const uint32_t c = base + (uint32_t)u8 * GT + threadIdx.x;
             if (c < n) {
                 const uint32_t lr = c / cpr, off = c - lr * cpr;
-                const int32_t v = __ldcg(gslot + q + nq * lr);
-                reinterpret_cast<uint4*>(db + (size_t)v * L.E)[off] = val[u];
+                const int32_t slot = __ldcg(ob + __ldcg(gsel + q + nq * lr));
+                reinterpret_cast<uint4*>(db + (size_t)slot * L.E)[off] = val[u8];
             }
         }
     }
@@ -585,24 +590,24 @@ __device__ __forceinline__ void fetch_rows(const Layout& L, int b, uint32_t q, u
 
 // Request b's fetch by nq CTAs (this one is share q). The CTA's own counter for
 // (b, q) gives the call's tag and advances once the share is done.
-__device__ __forceinline__ void fetch_request(const Layout& L, int b, uint32_t q, uint32_t nq, bool sync,
-                                              uint32_t* bcast) {
+__device__ __forceinline__ void fetch_request(const Layout& L, const int32_t* out, int k, int b, uint32_t q,
+                                              uint32_t nq, bool sync, uint32_t* bcast) {
     uint32_t* count = L.gcount + b + (size_t)q * L.R;
     const uint32_t ready = ld_relaxed(count) + 1u;
-    fetch_rows(L, b, q, nq, ready, sync, bcast);
+    fetch_rows(L, out, k, b, q, nq, ready, sync, bcast);
     __syncthreads();
     if (threadIdx.x == 0) *count = ready;
 }
 
 __global__ void __launch_bounds__(kGatherThreads, kGatherCtasPerSm)
-gather_kernel(const Layout L, int sync) {
+gather_kernel(const Layout L, const int32_t* __restrict__ out, int k, int sync) {
     __shared__ uint32_t bcast[2];
     const uint32_t G = gridDim.x, c = blockIdx.x, R = (uint32_t)L.R;
     if (G >= R) {  // several CTAs share each request
         const uint32_t b = c % R;
-        fetch_request(L, (int)b, c / R, (G - 1 - b) / R + 1, sync != 0, bcast);
+        fetch_request(L, out, k, (int)b, c / R, (G - 1 - b) / R + 1, sync != 0, bcast);
     } else {  // each CTA takes whole requests
-        for (uint32_t b = c; b < R; b += G) fetch_request(L, (int)b, 0, 1, sync != 0, bcast);
+        for (uint32_t b = c; b < R; b += G) fetch_request(L, out, k, (int)b, 0, 1, sync != 0, bcast);
     }
 }
 
@@ -623,8 +628,8 @@ void carve_miss_area(Layout& L, void* base) {
     uint8_t* p = static_cast<uint8_t*>(base);
     const size_t list = ((size_t)L.R * L.S * 4 + 15) & ~(size_t)15;
     const size_t per = ((size_t)L.R * 4 + 15) & ~(size_t)15;
-    L.mpos = reinterpret_cast<int32_t*>(p);
-    L.mslot = reinterpret_cast<int32_t*>(p + list);
+    L.fpos = reinterpret_cast<int32_t*>(p);
+    L.fsel = reinterpret_cast<int32_t*>(p + list);
     p += 2 * list;
     L.ready_pos = reinterpret_cast<uint32_t*>(p);
     L.ready_slot = reinterpret_cast<uint32_t*>(p + per);
@@ -650,7 +655,8 @@ cudaError_t launch_resolve(const Layout& L, cudaStream_t stream, const int32_t* 
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const Layout& L, cudaStream_t stream, int num_sms, bool pdl) {
+cudaError_t launch_gather(const Layout& L, cudaStream_t stream, const int32_t* out_slots, int k, int num_sms,
+                          bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(num_sms * kGatherCtasPerSm));
     cfg.blockDim = dim3(kGatherThreads);
@@ -661,7 +667,7 @@ cudaError_t launch_gather(const Layout& L, cudaStream_t stream, int num_sms, boo
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gather_kernel, L, pdl ? 1 : 0);
+    return cudaLaunchKernelEx(&cfg, gather_kernel, L, out_slots, k, pdl ? 1 : 0);
 }
 
 }  // namespace hs

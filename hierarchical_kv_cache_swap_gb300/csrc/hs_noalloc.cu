@@ -115,7 +115,7 @@ extern "C" int hs_resolve_noalloc(hs_stream_t stream, int num_requests, int cont
     // Callers with different sizes share this array, so the fetch CTAs' call counters
     // need not line up with a caller's requests: the fetch therefore runs after the
     // resolution here (no overlap) and reads the hand-off without waiting on flags.
-    if ((e = hs::launch_gather(L, s, d->num_sms, false)) != cudaSuccess)
+    if ((e = hs::launch_gather(L, s, out_slots, k, d->num_sms, false)) != cudaSuccess)
         return noalloc_fail(HS_ERR_CUDA, cudaGetErrorString(e));
     hs::record_error("");
     return HS_OK;
