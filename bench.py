@@ -306,6 +306,11 @@ def run_ours(args, rank: int, world: int, dist) -> None:
             ctx.resolve_host(sel_pin[t].numpy(), out_np, miss_np)
             e2e_s += time.perf_counter() - t0
 
+        # ---- decode-time append: one new entry per request per call (last, it rewrites rows)
+        append = None
+        if not args.no_extras and rank == 0:
+            append = measure_append(torch, ctx, w, flush, K)
+
         # ---- no-IO: all-hit resolution at 64 requests x k = 2048 (S = 4096)
         noio = None
         if not args.no_extras and rank == 0:
@@ -374,6 +379,7 @@ def run_ours(args, rank: int, world: int, dist) -> None:
         "misses_per_step": float(miss.sum()) / K,
         "kernels": kernels,
         "no_io": noio,
+        "append": append,
         "roofline": roofline,
         "gpu_launches": K * kpc,
         "device_status": status,
@@ -477,6 +483,29 @@ def run_layers(args, rank: int, world: int, dist) -> None:
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def measure_append(torch, ctx, w, flush, n: int) -> dict:
+    """hs_append of one E-byte row per request per call at uniform random positions
+    (those that are resident, about S / C of them, also write their slot), L2 flushed
+    between calls."""
+    g = torch.Generator().manual_seed(11)
+    pos = torch.randint(0, w.C, (n, w.B), generator=g, dtype=torch.int32).cuda()
+    rows = torch.randint(0, 256, (n, w.B, w.E), generator=g, dtype=torch.uint8).cuda()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    ctx.clear_status()
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record()
+        ctx.append(rows[i], pos[i])
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    us = [a.elapsed_time(b) * 1e3 for a, b in evs]
+    assert ctx.status() == 0
+    link = w.B * w.E
+    return {"calls": n, "rows_per_call": w.B, "link_bytes_per_call": link,
+            "us_per_call": statistics.mean(us), "us_per_call_median": statistics.median(us),
+            "link_gbs": link / (statistics.mean(us) * 1e-6) / 1e9}
 
 
 def measure_noio(torch, hs, tracegen, flush) -> dict:

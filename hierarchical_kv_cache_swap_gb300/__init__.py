@@ -35,6 +35,7 @@ SIGNATURES = {
     "hs_create": (_VP, [_I, _I, _I, _I]),
     "hs_create_with_host": (_VP, [_I, _I, _I, _I, _VP, _SZ]),
     "hs_checksum_rows": (_I, [_VP, _VP, _VP, _I, _I, _VP]),
+    "hs_append": (_I, [_VP, _VP, _VP, _VP, _I]),
     "hs_resolve": (_I, [_VP, _VP, _VP, _I, _I, _VP, _VP]),
     "hs_resolve_host": (_I, [_VP, _VP, _VP, _I, _I, _VP, _VP]),
     "hs_resolve_profiled": (_I, [_VP, _VP, _VP, _I, _I, _VP, _VP, _VP]),
@@ -194,6 +195,12 @@ class Context:
         B, k = out_slots.shape
         self._check(self._lib.hs_checksum_rows(self._h, _stream(stream), _addr(out_slots), B, k,
                                                _addr(sums)), "hs_checksum_rows")
+
+    def append(self, kv, positions, stream=None) -> None:
+        """Decode-time append: kv uint8 [R, E] and positions int32 [R] (device; negative =
+        no new entry) into the host store (and resident slots)."""
+        self._check(self._lib.hs_append(self._h, _stream(stream), _addr(kv), _addr(positions),
+                                        positions.shape[0]), "hs_append")
 
     def reset(self, stream=None) -> None:
         self._check(self._lib.hs_reset(self._h, _stream(stream)), "hs_reset")

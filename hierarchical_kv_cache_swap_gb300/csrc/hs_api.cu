@@ -238,6 +238,18 @@ hs_ctx* hs_create_with_host(int num_requests, int context_len, int slots, int en
     return create(num_requests, context_len, slots, entry_bytes, host_kv, host_stride);
 }
 
+int hs_append(hs_ctx* h, hs_stream_t stream, const uint8_t* kv, const int32_t* positions, int B) {
+    if (!h) return fail(HS_ERR_INVALID, "null context");
+    if (!kv || !positions) return fail(HS_ERR_INVALID, "null kv/positions");
+    if (B != h->L.R) return fail(HS_ERR_INVALID, "B=%d but the context has %d requests", B, h->L.R);
+    if ((uintptr_t)kv & 15) return fail(HS_ERR_INVALID, "kv must be 16-byte aligned");
+    if (B > 65535) return fail(HS_ERR_LIMIT, "hs_append handles at most 65535 requests");
+    cudaError_t e = hs::launch_append(h->L, (cudaStream_t)stream, kv, positions);
+    if (e != cudaSuccess) return cuda_fail(e, "append kernel launch");
+    g_err[0] = 0;
+    return HS_OK;
+}
+
 int hs_checksum_rows(hs_ctx* h, hs_stream_t stream, const int32_t* out_slots, int B, int k, uint64_t* sums) {
     if (!h) return fail(HS_ERR_INVALID, "null context");
     if (!out_slots || !sums) return fail(HS_ERR_INVALID, "null out_slots/sums");

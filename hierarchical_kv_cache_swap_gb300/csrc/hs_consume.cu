@@ -1,4 +1,4 @@
-// hs_consume.cu -- a stand-in for the sparse-attention consumer of resolved slots.
+// hs_consume.cu -- the consumer stand-in and the decode-time append around the step.
 //
 // HiSparse's resolution leaves every selected entry in a device slot for the layer's
 // sparse attention to read (blog commentary, section two: a resident entry takes part
@@ -53,7 +53,44 @@ checksum_kernel(const uint8_t* __restrict__ dev, int S, int E, const int32_t* __
     }
 }
 
+constexpr int kAppendThreads = 256;
+
+// Decode-time append: row kv[b] joins request b's history at position pos[b] in the
+// host store (zero-copy stores over the host link) and, when that position is
+// resident, its device slot. Grid (parts, R); CTA (part, b) copies its share of the
+// row's 16-byte chunks.
+__global__ void __launch_bounds__(kAppendThreads)
+append_kernel(const Layout L, const uint8_t* __restrict__ kv, const int32_t* __restrict__ pos) {
+    const int b = blockIdx.y;
+    const int32_t p = __ldg(pos + b);
+    if (p < 0) return;  // no new entry for this request
+    if (p >= L.C) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(L.status, 1u /* HS_STATUS_RANGE */);
+        return;
+    }
+    const int32_t s = L.pt[(size_t)b * L.C + p];
+    const uint32_t cpr = (uint32_t)L.E >> 4;
+    const uint32_t per = (cpr + gridDim.x - 1) / gridDim.x;
+    const uint32_t c0 = blockIdx.x * per, c1 = min(c0 + per, cpr);
+    const uint4* src = reinterpret_cast<const uint4*>(kv + (size_t)b * L.E);
+    uint4* host = reinterpret_cast<uint4*>(const_cast<uint8_t*>(L.host) + ((size_t)b * L.C + p) * L.host_stride);
+    uint4* dev = s >= 0 ? reinterpret_cast<uint4*>(L.dev + ((size_t)b * L.S + s) * L.E) : nullptr;
+    for (uint32_t c = c0 + threadIdx.x; c < c1; c += kAppendThreads) {
+        const uint4 v = __ldg(src + c);
+        host[c] = v;
+        if (dev) dev[c] = v;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_append(const Layout& L, cudaStream_t stream, const uint8_t* kv, const int32_t* positions) {
+    const uint32_t cpr = (uint32_t)L.E >> 4;
+    uint32_t parts = (cpr + kAppendThreads * 4 - 1) / (kAppendThreads * 4);  // >= 4 chunks per thread
+    if (parts < 1) parts = 1;
+    append_kernel<<<dim3(parts, (unsigned)L.R), kAppendThreads, 0, stream>>>(L, kv, positions);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_checksum(const uint8_t* dev, int R, int S, int E, const int32_t* out_slots, int k,
                             unsigned long long* sums, int num_sms, cudaStream_t stream) {

@@ -76,6 +76,9 @@ cudaError_t launch_gather(const Layout& L, cudaStream_t stream, const int32_t* o
 cudaError_t launch_checksum(const uint8_t* dev, int R, int S, int E, const int32_t* out_slots, int k,
                             unsigned long long* sums, int num_sms, cudaStream_t stream);
 
+// Enqueue the decode-time append of kv[b] (device [R][E]) at positions[b] (device [R]).
+cudaError_t launch_append(const Layout& L, cudaStream_t stream, const uint8_t* kv, const int32_t* positions);
+
 // Set the calling thread's message for hs_last_error().
 void record_error(const char* msg);
 

@@ -138,6 +138,22 @@ int hs_resolve_profiled(hs_ctx* ctx, hs_stream_t stream, const int32_t* selectio
                         int32_t* out_slots, int32_t* miss_counts, hs_event_t ev[3]);
 
 /*
+ * hs_append -- decode-time append of new KV entries (blog commentary, opening: the KV
+ * that does not need to stay on the GPU is offloaded to host memory; paper abstract:
+ * each request's full KV history lives in host memory). Enqueues on `stream` a kernel
+ * that writes kv[b] (device, [B][entry_bytes], 16-byte aligned) into the host store at
+ * position positions[b] of request b (device int32 [B]; negative = no new entry for
+ * that request) -- the writes cross the host link from the GPU -- and, when that
+ * position is resident in a slot (a rewrite), into the slot as well, so the cache stays
+ * exact. The replacement state does not change: to make a new entry resident, select it
+ * in the next hs_resolve (or resolve it on its own). A position >= context_len sets
+ * HS_STATUS_RANGE and is skipped. B must equal num_requests (at most 65535). Stream
+ * ordered with hs_resolve on the same context. Returns HS_OK, HS_ERR_INVALID,
+ * HS_ERR_LIMIT or HS_ERR_CUDA.
+ */
+int hs_append(hs_ctx* ctx, hs_stream_t stream, const uint8_t* kv, const int32_t* positions, int B);
+
+/*
  * hs_checksum_rows -- a stand-in for the sparse-attention consumer of a layer (blog
  * commentary, section two: a resident entry takes part in the computation directly).
  * Enqueues on `stream` a kernel that reads the k rows each request resolved to, through

@@ -63,6 +63,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.orc_resolve_request.restype = i32
         lib.orc_resolve.argtypes = [vp, vp, sz, vp, i32, i32, vp, vp]
         lib.orc_resolve.restype = i32
+        lib.orc_append.argtypes = [vp, i32, vp, sz, i32, vp]
+        lib.orc_append.restype = i32
         _libs[path] = lib
     return lib
 
@@ -151,3 +153,17 @@ class Oracle:
         if rc < 0:
             raise ValueError(f"orc_resolve_request failed ({rc})")
         return out, int(miss[0]), rc
+
+    def append(self, host: np.ndarray, positions, rows: np.ndarray) -> int:
+        """Decode-time append for all R requests: host [R][C][stride] (written), positions
+        [R] (negative = none), rows [R][E]. Returns the OR of the status words."""
+        rows = np.ascontiguousarray(rows, dtype=np.uint8)
+        st = 0
+        for b in range(self.R):
+            hb = host[b]
+            rc = self._lib.orc_append(self._h, b, hb.ctypes.data, host.shape[2], int(positions[b]),
+                                      rows[b].ctypes.data)
+            if rc < 0:
+                raise ValueError(f"orc_append failed ({rc})")
+            st |= rc
+        return st

@@ -204,3 +204,25 @@ int orc_resolve(orc_state* o, const uint8_t* host, size_t host_stride, const int
     }
     return status;
 }
+
+/*
+ * Decode-time append (blog commentary, opening and section two: the KV the decode no
+ * longer needs on the GPU lives in host memory, which keeps each request's full
+ * history; paper abstract: the full KV history is kept in host memory). The new entry
+ * `row` of request b joins its history at position p: host_b[p] = row. If p is
+ * resident (a rewrite of an entry already in a slot), the slot gets the row too, so the
+ * cache stays exact. A negative p means no new entry; p >= C is a range error. The
+ * replacement state (page table, stamps, steps) does not change: admitting the new
+ * entry into a slot is a resolution that selects it.
+ * Returns 0, ORC_ERR_RANGE, or a negative error.
+ */
+int orc_append(orc_state* o, int b, uint8_t* host_b, size_t host_stride, int32_t p, const uint8_t* row) {
+    if (!o || b < 0 || b >= o->R || !host_b || !row) return ORC_EINVAL;
+    if (p < 0) return 0;
+    if (p >= o->C) return ORC_ERR_RANGE;
+    memcpy(host_b + (size_t)p * host_stride, row, (size_t)o->E);
+    const int32_t s = o->pt[(size_t)b * o->C + p];
+    if (s >= 0) memcpy(o->dev + ((size_t)b * o->S + s) * o->E, row, (size_t)o->E);
+    return 0;
+}
+

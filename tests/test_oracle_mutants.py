@@ -23,12 +23,14 @@ MUTANTS = {
     "most_recent_victim": ("int32_t v = V[i].slot;", "int32_t v = V[nv - 1 - i].slot;"),
     "step_not_advanced": ("o->t[b] = t + 1;", "o->t[b] = t;"),
     "duplicate_miss_counted_twice": ("*miss_b = m;", "*miss_b = np;"),
+    "append_skips_resident_slot": ("if (s >= 0) memcpy(o->dev + ((size_t)b * o->S + s) * o->E, row, (size_t)o->E);", ""),
     "most_recent_first_order": ("if (x->lu != y->lu) return (x->lu > y->lu) - (x->lu < y->lu);",
                                 "if (x->lu != y->lu) return (x->lu < y->lu) - (x->lu > y->lu);"),
 }
 
 
 def _pin_suite(Oracle, path):
+    pins.run_append(Oracle, path)
     pins.run_hand_trace(Oracle, path)
     pins.run_textbook_k1(Oracle, path, seeds=range(3))
     pins.run_list_model_random(Oracle, path, seeds=range(4), steps=25)

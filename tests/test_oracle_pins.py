@@ -353,3 +353,32 @@ def test_noio_trace_is_all_hits_after_first_call(oracle_mod, tg):
     for t in range(6):
         _, m, _ = o.resolve(host, 16, sel[t])
         assert (m == (w.k if t == 0 else 0)).all()
+
+
+# --------------------------------------------------------------------- decode-time append
+
+def run_append(Oracle, lib_path=None, ERR_RANGE=1):
+    """An appended entry is part of the host history (a later miss fetches it), and a
+    rewrite of a resident entry reaches its slot at once (the consumer view stays exact)."""
+    C, S, E = 32, 4, 16
+    host = _host(1, C, E, 5)
+    o = Oracle(1, C, S, E, lib_path=lib_path)
+    new = np.full((1, E), 0xAB, dtype=np.uint8)
+    assert o.append(host, [30], new) == 0           # not resident: host only
+    assert (host[0, 30] == 0xAB).all()
+    out, m, _ = o.resolve(host, E, np.array([[30, 2]], dtype=np.int32))
+    assert m[0] == 2 and (o.dev[0, out[0, 0]] == 0xAB).all()
+    new2 = np.full((1, E), 0x5C, dtype=np.uint8)
+    state = (o.pt.copy(), o.tok.copy(), o.lu.copy(), o.t.copy())
+    assert o.append(host, [2], new2) == 0            # resident: host and slot
+    assert (host[0, 2] == 0x5C).all() and (o.dev[0, out[0, 1]] == 0x5C).all()
+    for a, b_ in zip(state, (o.pt, o.tok, o.lu, o.t)):
+        assert (a == b_).all()                      # replacement state untouched
+    out2, m2, _ = o.resolve(host, E, np.array([[2, 30]], dtype=np.int32))
+    assert m2[0] == 0 and (o.dev[0, out2[0, 0]] == 0x5C).all()
+    assert o.append(host, [-1], new) == 0            # no new entry
+    assert o.append(host, [C], new) == ERR_RANGE
+
+
+def test_append_joins_the_history_and_keeps_the_cache_exact(oracle_mod):
+    run_append(oracle_mod.Oracle, None, oracle_mod.ERR_RANGE)
