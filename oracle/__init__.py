@@ -26,6 +26,7 @@ LIB = os.path.join(_HERE, "libhs_oracle.so")
 
 ERR_RANGE = 1
 ERR_DUP = 2
+POLICY_LRU, POLICY_FIFO, POLICY_RANDOM = 0, 1, 2
 
 
 def compile_oracle(src: str, out: str) -> str:
@@ -65,12 +66,31 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.orc_resolve.restype = i32
         lib.orc_append.argtypes = [vp, i32, vp, sz, i32, vp]
         lib.orc_append.restype = i32
+        u64 = ctypes.c_uint64
+        lib.orc_set_policy.argtypes = [vp, i32, u64]
+        lib.orc_set_policy.restype = i32
+        lib.orc_set_request_id.argtypes = [vp, i32, i32]
+        lib.orc_set_request_id.restype = i32
+        lib.orc_splitmix64.argtypes = [u64, u64]
+        lib.orc_splitmix64.restype = u64
+        lib.orc_random_key.argtypes = [u64, i32, i32, i32]
+        lib.orc_random_key.restype = ctypes.c_uint32
         _libs[path] = lib
     return lib
 
 
 def _ptr(a: np.ndarray) -> int:
     return a.ctypes.data
+
+
+def splitmix64(x: int, n: int) -> int:
+    """SplitMix64 output number n of the generator seeded with x (the oracle's C)."""
+    return int(load().orc_splitmix64(x & (2**64 - 1), n & (2**64 - 1)))
+
+
+def random_key(seed: int, b: int, t: int, s: int) -> int:
+    """The RANDOM policy's key of slot s at call t of request b (the oracle's C)."""
+    return int(load().orc_random_key(seed & (2**64 - 1), b, t, s))
 
 
 class Oracle:
@@ -82,6 +102,17 @@ class Oracle:
         self._h = self._lib.orc_create(R, C, S, E)
         if not self._h:
             raise MemoryError("orc_create failed")
+
+    def set_policy(self, policy: int, seed: int = 0) -> None:
+        """Replacement policy (POLICY_LRU / FIFO / RANDOM) for the calls that follow."""
+        if self._lib.orc_set_policy(self._h, policy, seed & (2**64 - 1)) != 0:
+            raise ValueError(f"orc_set_policy({policy}) refused")
+
+    def set_request_ids(self, ids) -> None:
+        """Row b of this state stands for request ids[b] (RANDOM draws depend on it)."""
+        for b, i in enumerate(ids):
+            if self._lib.orc_set_request_id(self._h, b, int(i)) != 0:
+                raise ValueError("orc_set_request_id refused")
 
     def close(self) -> None:
         if self._h:

@@ -30,10 +30,28 @@
  *   - a position repeated within one row resolves to the same slot each time and
  *     counts once (misses are a set of positions); the status gets ORC_ERR_DUP.
  *
+ * Replacement policies. LRU (above) is the method's policy; the blog commentary's
+ * section on Fig. 3 compares it with policies that do not exploit locality, which
+ * the pages do not name. Two such variants are kept for that comparison, each read
+ * as the plainest policy of its kind:
+ *   - FIFO: the stamp of a slot is the call that filled it; a hit does not restamp,
+ *     so the victims are the non-hit slots in ascending (fill call, slot) order;
+ *   - RANDOM: the victims are the non-hit slots in ascending (key, slot) order, the
+ *     key of slot s at call t of request b being the high 32 bits of SplitMix64
+ *     output number (t * 2^16 + s) of the stream whose seed is SplitMix64 output
+ *     number b of the policy seed (Steele, Lea and Flood, "Fast splittable
+ *     pseudorandom number generators", 2014: output n of seed x is
+ *     mix(x + (n + 1) * 0x9E3779B97F4A7C15) with the 13th of Stafford's mixers);
+ *     stamps are kept as under LRU. It needs S <= 65536.
+ * Hits, misses, the miss order, pairing and page-table updates are the same for all.
+ *
  * Parity is pinned (not to this code itself) by: a hand-worked trace, a textbook
  * single-access LRU cache (k = 1), an independently written recency-list LRU,
  * closed forms for the cold start, for S >= C and for S = k, the per-step miss
- * bound k - floor(keep * k), and the invariants of an exact cache.
+ * bound k - floor(keep * k), and the invariants of an exact cache. The variants
+ * are pinned by Belady's textbook string (FIFO and LRU fault counts), a textbook
+ * FIFO queue, SplitMix64's published outputs with victims recomputed from them, the
+ * uniformity of RANDOM's victims, and the loop of S + 1 positions.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -44,6 +62,9 @@
 #define ORC_ERR_DUP 2u
 #define ORC_EINVAL (-1)
 #define ORC_ENOMEM (-2)
+#define ORC_POLICY_LRU 0
+#define ORC_POLICY_FIFO 1
+#define ORC_POLICY_RANDOM 2
 
 typedef struct {
     int R, C, S, E;
@@ -52,6 +73,9 @@ typedef struct {
     int32_t* lu;  /* [R][S]    last-use stamp, -1 when never used     */
     int32_t* t;   /* [R]       calls made so far for the request      */
     uint8_t* dev; /* [R][S][E] contents of the device slots           */
+    int32_t* rid; /* [R]       request number of each row (RANDOM keys) */
+    int policy;   /* ORC_POLICY_*, LRU unless set                     */
+    uint64_t seed;/* the RANDOM policy's seed                         */
 } orc_state;
 
 orc_state* orc_create(int R, int C, int S, int E) {
@@ -64,10 +88,12 @@ orc_state* orc_create(int R, int C, int S, int E) {
     o->lu = (int32_t*)malloc(sizeof(int32_t) * (size_t)R * S);
     o->t = (int32_t*)calloc((size_t)R, sizeof(int32_t));
     o->dev = (uint8_t*)calloc((size_t)R * S, (size_t)E);
-    if (!o->pt || !o->tok || !o->lu || !o->t || !o->dev) {
-        free(o->pt); free(o->tok); free(o->lu); free(o->t); free(o->dev); free(o);
+    o->rid = (int32_t*)malloc(sizeof(int32_t) * (size_t)R);
+    if (!o->pt || !o->tok || !o->lu || !o->t || !o->dev || !o->rid) {
+        free(o->pt); free(o->tok); free(o->lu); free(o->t); free(o->dev); free(o->rid); free(o);
         return NULL;
     }
+    for (int b = 0; b < R; ++b) o->rid[b] = b;
     for (size_t i = 0; i < (size_t)R * C; ++i) o->pt[i] = -1;
     for (size_t i = 0; i < (size_t)R * S; ++i) { o->tok[i] = -1; o->lu[i] = -1; }
     return o;
@@ -75,7 +101,38 @@ orc_state* orc_create(int R, int C, int S, int E) {
 
 void orc_destroy(orc_state* o) {
     if (!o) return;
-    free(o->pt); free(o->tok); free(o->lu); free(o->t); free(o->dev); free(o);
+    free(o->pt); free(o->tok); free(o->lu); free(o->t); free(o->dev); free(o->rid); free(o);
+}
+
+/* Replacement policy for the calls that follow (the state kept so far carries over). */
+int orc_set_policy(orc_state* o, int policy, uint64_t seed) {
+    if (!o || policy < ORC_POLICY_LRU || policy > ORC_POLICY_RANDOM) return ORC_EINVAL;
+    if (policy == ORC_POLICY_RANDOM && o->S > 65536) return ORC_EINVAL;
+    o->policy = policy;
+    o->seed = seed;
+    return 0;
+}
+
+/* Row b of this state follows request number id of a larger batch (the RANDOM
+ * policy's draws depend on the request number; the default is b). */
+int orc_set_request_id(orc_state* o, int b, int32_t id) {
+    if (!o || b < 0 || b >= o->R || id < 0) return ORC_EINVAL;
+    o->rid[b] = id;
+    return 0;
+}
+
+/* SplitMix64 output number n (n = 0, 1, 2, ...) of the generator seeded with x. */
+uint64_t orc_splitmix64(uint64_t x, uint64_t n) {
+    uint64_t z = x + (n + 1u) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+/* The RANDOM policy's key of slot s at call t of request b. */
+uint32_t orc_random_key(uint64_t seed, int b, int32_t t, int s) {
+    const uint64_t stream = orc_splitmix64(seed, (uint64_t)b);
+    return (uint32_t)(orc_splitmix64(stream, ((uint64_t)(uint32_t)t << 16) + (uint64_t)s) >> 32);
 }
 
 int32_t* orc_pt(orc_state* o) { return o->pt; }
@@ -90,12 +147,12 @@ static int cmp_int(const void* a, const void* b) {
     return (x > y) - (x < y);
 }
 
-typedef struct { int32_t lu, slot; } cand_t;
+typedef struct { int64_t key; int32_t slot; } cand_t;
 
 static int cmp_cand(const void* a, const void* b) {
     const cand_t* x = (const cand_t*)a;
     const cand_t* y = (const cand_t*)b;
-    if (x->lu != y->lu) return (x->lu > y->lu) - (x->lu < y->lu);
+    if (x->key != y->key) return (x->key > y->key) - (x->key < y->key);
     return (x->slot > y->slot) - (x->slot < y->slot);
 }
 
@@ -154,11 +211,12 @@ int orc_resolve_request(orc_state* o, int b, const uint8_t* host_b, size_t host_
         free(Q);
     }
 
-    /* 3. LRU order of the slots not hit in this call: ascending (last_use, slot) */
+    /* 3. eviction order of the slots not hit in this call: ascending (key, slot), the
+     *    key being the stamp (LRU: last use; FIFO: fill) or the RANDOM policy's draw */
     int nv = 0;
     for (int s = 0; s < S; ++s) {
         if (hit[s]) continue;
-        V[nv].lu = lu[s];
+        V[nv].key = o->policy == ORC_POLICY_RANDOM ? (int64_t)orc_random_key(o->seed, o->rid[b], t, s) : (int64_t)lu[s];
         V[nv].slot = s;
         ++nv;
     }
@@ -177,8 +235,9 @@ int orc_resolve_request(orc_state* o, int b, const uint8_t* host_b, size_t host_
         if (p >= 0 && p < C && out_b[j] < 0) out_b[j] = pt[p];
     }
 
-    /* 5. stamps and counters */
-    for (int s = 0; s < S; ++s) if (hit[s]) lu[s] = t;
+    /* 5. stamps and counters (FIFO keeps the fill call of a hit slot) */
+    if (o->policy != ORC_POLICY_FIFO)
+        for (int s = 0; s < S; ++s) if (hit[s]) lu[s] = t;
     for (int i = 0; i < m; ++i) lu[V[i].slot] = t;
     *miss_b = m;
     o->t[b] = t + 1;

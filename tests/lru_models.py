@@ -83,3 +83,36 @@ class RecencyListLRU:
         for p, s in self.slot_of.items():
             pt[p] = s
         return pt
+
+
+class TextbookFIFO:
+    """A classic single-access FIFO cache of `capacity` entries (a queue of arrivals;
+    a hit changes nothing)."""
+
+    def __init__(self, capacity: int):
+        self.capacity = capacity
+        self.q: list[int] = []
+
+    def access(self, x: int) -> bool:
+        """Returns True on a miss."""
+        if x in self.q:
+            return False
+        if len(self.q) == self.capacity:
+            self.q.pop(0)
+        self.q.append(x)
+        return True
+
+    def resident(self) -> set[int]:
+        return set(self.q)
+
+
+_M64 = (1 << 64) - 1
+
+
+def splitmix64(x: int, n: int) -> int:
+    """Output number n (0, 1, ...) of SplitMix64 seeded with x, from its published
+    definition (Steele, Lea and Flood 2014; Stafford's 13th mixer)."""
+    z = (x + (n + 1) * 0x9E3779B97F4A7C15) & _M64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & _M64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _M64
+    return z ^ (z >> 31)

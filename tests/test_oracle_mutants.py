@@ -24,12 +24,18 @@ MUTANTS = {
     "step_not_advanced": ("o->t[b] = t + 1;", "o->t[b] = t;"),
     "duplicate_miss_counted_twice": ("*miss_b = m;", "*miss_b = np;"),
     "append_skips_resident_slot": ("if (s >= 0) memcpy(o->dev + ((size_t)b * o->S + s) * o->E, row, (size_t)o->E);", ""),
-    "most_recent_first_order": ("if (x->lu != y->lu) return (x->lu > y->lu) - (x->lu < y->lu);",
-                                "if (x->lu != y->lu) return (x->lu < y->lu) - (x->lu > y->lu);"),
+    "most_recent_first_order": ("if (x->key != y->key) return (x->key > y->key) - (x->key < y->key);",
+                                "if (x->key != y->key) return (x->key < y->key) - (x->key > y->key);"),
+    "fifo_restamps_hits": ("if (o->policy != ORC_POLICY_FIFO)\n", "if (1)\n"),
+    "random_key_low_bits": ("+ (uint64_t)s) >> 32);", "+ (uint64_t)s));"),
+    "random_key_ignores_request": ("orc_random_key(o->seed, o->rid[b], t, s)", "orc_random_key(o->seed, b, t, s)"),
+    "random_counter_swapped": ("((uint64_t)(uint32_t)t << 16) + (uint64_t)s", "((uint64_t)(uint32_t)s << 16) + (uint64_t)t"),
+    "random_policy_uses_stamps": ("o->policy == ORC_POLICY_RANDOM ?", "o->policy == -7 ?"),
 }
 
 
 def _pin_suite(Oracle, path):
+    pins.run_policies(Oracle, path)
     pins.run_append(Oracle, path)
     pins.run_hand_trace(Oracle, path)
     pins.run_textbook_k1(Oracle, path, seeds=range(3))

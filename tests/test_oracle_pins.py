@@ -19,7 +19,7 @@ import random
 import numpy as np
 import pytest
 
-from tests.lru_models import RecencyListLRU, TextbookLRU
+from tests.lru_models import RecencyListLRU, TextbookFIFO, TextbookLRU, splitmix64
 
 pytestmark = pytest.mark.filterwarnings("ignore")
 
@@ -382,3 +382,120 @@ def run_append(Oracle, lib_path=None, ERR_RANGE=1):
 
 def test_append_joins_the_history_and_keeps_the_cache_exact(oracle_mod):
     run_append(oracle_mod.Oracle, None, oracle_mod.ERR_RANGE)
+
+
+# --------------------------------------------------------------------- replacement policies
+# LRU is the method's policy; FIFO and RANDOM are the locality-blind comparisons of the
+# blog commentary's Fig. 3 discussion (the pages name neither; both are read as the
+# plainest policy of their kind).
+
+LRU, FIFO, RANDOM = 0, 1, 2
+
+# The textbook reference string of Belady's anomaly, one access per call.
+BELADY = [1, 2, 3, 4, 1, 2, 5, 1, 2, 3, 4, 5]
+
+
+def _calls(o, host, rows):
+    outs, misses = [], []
+    for sel in rows:
+        out, m, _ = o.resolve(host, host.shape[2], np.asarray(sel, dtype=np.int32).reshape(o.R, -1))
+        outs.append(out)
+        misses.append(m)
+    return outs, misses
+
+
+def run_policies(Oracle, lib_path=None):
+    E = 16
+    # (1) Belady's string: FIFO faults 9 times with 3 frames and 10 with 4; LRU 10 and 8
+    for policy, S, faults in ((FIFO, 3, 9), (FIFO, 4, 10), (LRU, 3, 10), (LRU, 4, 8)):
+        o = Oracle(1, 8, S, E, lib_path=lib_path)
+        o.set_policy(policy)
+        _, m = _calls(o, _host(1, 8, E), [[x] for x in BELADY])
+        assert int(np.sum(m)) == faults, (policy, S)
+    # (2) FIFO against a textbook FIFO queue on random single-access traces; the stamp of
+    #     every occupied slot is the call that filled it
+    for seed in range(3):
+        rng = random.Random(seed)
+        C, S = rng.choice([(10, 3), (16, 5), (40, 7)])
+        host = _host(1, C, E, seed)
+        o = Oracle(1, C, S, E, lib_path=lib_path)
+        o.set_policy(FIFO)
+        ref = TextbookFIFO(S)
+        filled = [-1] * S
+        for t in range(150):
+            x = rng.randrange(C) if rng.random() < 0.5 else rng.randrange(max(1, C // 3))
+            out, m, _ = o.resolve(host, E, np.array([[x]], dtype=np.int32))
+            assert int(m[0]) == int(ref.access(x)), (seed, t)
+            if m[0]:
+                filled[out[0, 0]] = t
+            assert {int(p) for p in o.tok[0] if p >= 0} == ref.resident(), (seed, t)
+            assert o.lu[0].tolist() == filled, (seed, t)
+            assert (o.dev[0, out[0, 0]] == host[0, x]).all()
+    # (3) RANDOM: the victims of every call are the non-hit slots with the smallest
+    #     (key, slot), keys from SplitMix64 as published, request numbers honoured
+    seed = 0xC0FFEE
+    C, S, k, R = 64, 12, 4, 3
+    host = _host(R, C, E, 3)
+    o = Oracle(R, C, S, E, lib_path=lib_path)
+    o.set_policy(RANDOM, seed)
+    ids = [5, 0, 1 << 19]
+    o.set_request_ids(ids)
+    rng = np.random.default_rng(4)
+    for t in range(60):
+        sel = np.stack([rng.choice(C if t % 3 else 20, size=k, replace=False) for _ in range(R)]).astype(np.int32)
+        tok0 = o.tok.copy()
+        out, m, _ = o.resolve(host, E, sel)
+        for b in range(R):
+            hit = {int(s) for s in range(S) if tok0[b, s] >= 0 and tok0[b, s] in set(sel[b].tolist())}
+            stream = splitmix64(seed, ids[b])
+            cand = sorted((splitmix64(stream, (t << 16) + s) >> 32, s) for s in range(S) if s not in hit)
+            missed = sorted({int(p) for p in sel[b]} - {int(tok0[b, s]) for s in hit})
+            assert int(m[b]) == len(missed)
+            for p, (_, v) in zip(missed, cand):
+                assert int(o.pt[b, p]) == v and int(o.tok[b, v]) == p, (t, b)
+            for j, p in enumerate(sel[b]):
+                assert (o.dev[b, out[b, j]] == host[b, p]).all()
+    # (4) a loop over S + 1 positions: LRU and FIFO miss on every call (the textbook
+    #     pathology of recency and arrival order), RANDOM keeps some of the loop
+    S = 6
+    loop = [[x % (S + 1)] for x in range(20 * (S + 1))]
+    for policy, none_hit in ((LRU, True), (FIFO, True), (RANDOM, False)):
+        o = Oracle(1, S + 1, S, E, lib_path=lib_path)
+        o.set_policy(policy, 9)
+        _, m = _calls(o, _host(1, S + 1, E), loop)
+        hits = len(loop) - int(np.sum(m))
+        assert (hits == 0) == none_hit, (policy, hits)
+
+
+def test_replacement_policies(oracle_mod):
+    run_policies(oracle_mod.Oracle)
+
+
+def test_splitmix64_published_outputs(oracle_mod):
+    """SplitMix64's published outputs for seeds 0 and 1234567, for the test's model and
+    for the oracle's generator."""
+    want = {0: [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F],
+            1234567: [6457827717110365317, 3203168211198807973, 9817491932198370423,
+                      4593380528125082431, 16408922859458223821]}
+    for seed, outs in want.items():
+        for n, v in enumerate(outs):
+            assert splitmix64(seed, n) == v
+            assert oracle_mod.splitmix64(seed, n) == v
+    assert oracle_mod.random_key(7, 3, 11, 5) == splitmix64(splitmix64(7, 3), (11 << 16) + 5) >> 32
+
+
+def test_random_victims_are_uniform(oracle_mod):
+    """With every call a miss on a full cache, each of the S slots is the victim about
+    equally often (chi-square, 7 degrees of freedom, below the 0.1 % quantile 24.3)."""
+    S, n = 8, 4000
+    o = oracle_mod.Oracle(1, n + S, S, 16)
+    o.set_policy(RANDOM, 12345)
+    host = _host(1, n + S, 16)
+    counts = np.zeros(S)
+    for x in range(n + S):
+        out, m, _ = o.resolve(host, 16, np.array([[x]], dtype=np.int32))
+        assert m[0] == 1
+        if x >= S:
+            counts[out[0, 0]] += 1
+    chi2 = float(((counts - n / S) ** 2 / (n / S)).sum())
+    assert chi2 < 24.3, counts
