@@ -306,6 +306,11 @@ def run_ours(args, rank: int, world: int, dist) -> None:
             ctx.resolve_host(sel_pin[t].numpy(), out_np, miss_np)
             e2e_s += time.perf_counter() - t0
 
+        # ---- replacement policies: the step under each, and misses over buffer sizes
+        policies = None
+        if not args.no_extras and rank == 0:
+            policies = measure_policies(torch, hs, ctx, w, sel_dev, out_dev, miss_dev, flush, W, K)
+
         # ---- decode-time append: one new entry per request per call (last, it rewrites rows)
         append = None
         if not args.no_extras and rank == 0:
@@ -380,6 +385,7 @@ def run_ours(args, rank: int, world: int, dist) -> None:
         "kernels": kernels,
         "no_io": noio,
         "append": append,
+        "policies": policies,
         "roofline": roofline,
         "gpu_launches": K * kpc,
         "device_status": status,
@@ -483,6 +489,53 @@ def run_layers(args, rank: int, world: int, dist) -> None:
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+POLICIES = (("lru", 0), ("fifo", 1), ("random", 2))
+POLICY_SEED = 0x5EED
+
+
+def measure_policies(torch, hs, ctx, w, sel_dev, out_dev, miss_dev, flush, W: int, K: int) -> dict:
+    """The timed steps again under each replacement policy (L2 flushed between steps,
+    like the main pass), then the misses per step over buffer sizes S on the same
+    trace (bookkeeping only: HS_FLAG_NO_COPY, the first, cold call left out)."""
+    stream = torch.cuda.current_stream()
+    step = {}
+    for name, pol in POLICIES:
+        ctx.set_policy(pol, POLICY_SEED)
+        ctx.reset()
+        for t in range(W):
+            ctx.resolve(sel_dev[t], out_dev[t], miss_dev[t])
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            ctx.resolve(sel_dev[W + i], out_dev[W + i], miss_dev[W + i])
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        us = [a.elapsed_time(b) * 1e3 for a, b in ev]
+        step[name] = {"us_per_layer_step": statistics.mean(us), "us_median": statistics.median(us),
+                      "misses_per_step": float(miss_dev[W:].sum()) / K}
+    ctx.set_policy(0)
+    T = min(W + K, 128)
+    curve = {}
+    for S in (w.k, w.k * 3 // 2, 2 * w.k, 3 * w.k, 4 * w.k):
+        c = hs.Context(w.B, w.C, S, w.E, share_host_with=ctx)
+        c.set_flags(hs.HS_FLAG_NO_COPY)
+        m = torch.empty((T, w.B), dtype=torch.int32, device="cuda")
+        row = {}
+        for name, pol in POLICIES:
+            c.set_policy(pol, POLICY_SEED)
+            c.reset()
+            for t in range(T):
+                c.resolve(sel_dev[t], out_dev[t], m[t])
+            torch.cuda.synchronize()
+            row[name] = float(m[1:].sum()) / (T - 1)
+        c.close()
+        curve[str(S)] = row
+    return {"step": step, "misses_per_step_by_slots": curve, "trace_steps_for_curve": T,
+            "seed": POLICY_SEED}
 
 
 def measure_append(torch, ctx, w, flush, n: int) -> dict:

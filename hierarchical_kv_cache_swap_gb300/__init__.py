@@ -28,6 +28,7 @@ HS_STATUS_DUP = 2
 HS_STATUS_STEP_LIMIT = 4
 HS_STATUS_TIMEOUT = 8
 HS_FLAG_NO_COPY = 1
+POLICY_LRU, POLICY_FIFO, POLICY_RANDOM = 0, 1, 2
 
 # every symbol include/hs.h declares, with (restype, argtypes)
 _VP, _I, _SZ, _U = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint
@@ -51,6 +52,7 @@ SIGNATURES = {
     "hs_get_status": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "hs_clear_status": (_I, [_VP]),
     "hs_set_flags": (_I, [_VP, _U]),
+    "hs_set_policy": (_I, [_VP, _I, ctypes.c_uint64]),
     "hs_kernels_per_call": (_I, [_VP]),
     "hs_last_error": (ctypes.c_char_p, []),
     "hs_resolve_noalloc": (_I, [_VP, _I, _I, _I, _I, _VP, _SZ, _VP, _VP, _VP, _VP, _VP, _VP, _I,
@@ -207,6 +209,10 @@ class Context:
 
     def set_flags(self, flags: int) -> None:
         self._check(self._lib.hs_set_flags(self._h, flags), "hs_set_flags")
+
+    def set_policy(self, policy: int, seed: int = 0) -> None:
+        """Replacement policy (POLICY_LRU / POLICY_FIFO / POLICY_RANDOM) of later calls."""
+        self._check(self._lib.hs_set_policy(self._h, policy, seed & (2**64 - 1)), "hs_set_policy")
 
     def kernels_per_call(self) -> int:
         return int(self._lib.hs_kernels_per_call(self._h))

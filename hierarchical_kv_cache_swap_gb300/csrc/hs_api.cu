@@ -353,6 +353,15 @@ int hs_set_flags(hs_ctx* h, unsigned flags) {
     return HS_OK;
 }
 
+int hs_set_policy(hs_ctx* h, int policy, uint64_t seed) {
+    if (!h) return fail(HS_ERR_INVALID, "null context");
+    if (policy != HS_POLICY_LRU && policy != HS_POLICY_FIFO && policy != HS_POLICY_RANDOM)
+        return fail(HS_ERR_INVALID, "unknown policy %d", policy);
+    h->L.policy = policy;
+    h->L.seed = seed;
+    return HS_OK;
+}
+
 int hs_kernels_per_call(hs_ctx* h) {
     if (!h) return fail(HS_ERR_INVALID, "null context");
     return (h->flags & HS_FLAG_NO_COPY) ? 1 : 2;

@@ -25,6 +25,11 @@ constexpr unsigned kPollSleepNs = 32;              // first pause between polls 
 constexpr unsigned kPollSleepMaxNs = 256;          // doubling up to this (fewer polls, less L2 traffic)
 
 // Everything the two kernels need about one context.
+// Replacement policies (values of HS_POLICY_*).
+constexpr int kPolicyLru = 0;     // victims by ascending (last use, slot)
+constexpr int kPolicyFifo = 1;    // victims by ascending (fill call, slot); hits keep their stamp
+constexpr int kPolicyRandom = 2;  // victims by ascending (SplitMix64 draw, slot)
+
 struct Layout {
     int R, C, S, E;
     size_t host_stride;
@@ -41,6 +46,8 @@ struct Layout {
     uint32_t* ready_pos;   // [R]: (tag mod 2^16) << 16 | list length, once request b's list is published
     uint32_t* ready_slot;  // [R]: == tag once request b's answers (out_slots) are written
     uint32_t* gcount;      // [R + G]: fetch CTA counters; (b, share q) at b + q*R; tag = gcount[b] + 1
+    int policy = kPolicyLru;  // replacement policy of the calls launched with this layout
+    uint64_t seed = 0;        // kPolicyRandom's seed
 };
 
 // Bytes of the miss area for R requests of S slots, and its layout at `base`

@@ -15,7 +15,8 @@
 //      miss area as it finds it; right after the probe's barrier the list is
 //      PUBLISHED (ready_pos): the source rows of the fetch are known from here on;
 //   3. rank the misses by ascending position (a group prefix over the bitmap plus
-//      popcounts), rank the non-hit slots by (last_use, slot) with a stable LSD radix
+//      popcounts), rank the non-hit slots by (last_use, slot) -- or, under the
+//      comparison policies, by (fill call, slot) or (random draw, slot) -- with a stable LSD radix
 //      sort whose digits are counted per warp (__match_any_sync ranks equal digits
 //      inside a warp, an exclusive scan over the (digit, warp) table orders the warps),
 //      pair the r-th miss with the r-th victim and answer the missed selections; the
@@ -149,6 +150,17 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* s
     *total = scratch[BW];
     __syncthreads();
     return r;
+}
+
+// SplitMix64 output number n (n = 0, 1, ...) of the generator seeded with x (Steele,
+// Lea and Flood, "Fast splittable pseudorandom number generators", 2014: the state
+// advances by the golden-ratio increment and each output is Stafford's 13th mixer of
+// it), so any output is computed directly from (x, n): the RANDOM policy's draws.
+__device__ __forceinline__ uint64_t splitmix64(uint64_t x, uint64_t n) {
+    uint64_t z = x + (n + 1ull) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
 }
 
 // Shared-memory plan of one request's resolution (byte offsets).
@@ -288,7 +300,7 @@ struct Request {
                 if (ss >= 0) {  // hit: answered in place, stamped, not evictable
                     const uint32_t bit = 1u << (ss & 31);
                     if (atomicOr(&hitbm[ss >> 5], bit) & bit) st |= HS_STATUS_DUP;
-                    lub[ss] = t;
+                    if (L.policy != kPolicyFifo) lub[ss] = t;  // FIFO keeps the fill call
                     outb[j] = ss;
                 } else if (pp >= 0 && pp < C) {  // miss: marked, and listed for the fetch
                     const uint32_t bit = 1u << (pp & 31);
@@ -355,11 +367,15 @@ struct Request {
         __syncthreads();
     }
 
-    // 4a. LRU order of the non-hit slots: ascending (last_use, slot); sets victims.
+    // 4a. eviction order of the non-hit slots: ascending (key, slot), the key being the
+    // stamp + 1 (LRU: last use, FIFO: fill call) or the RANDOM policy's draw; sets victims.
     __device__ void rank_victims() {
         const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
         drain();  // the stamps copied at kernel start have landed (this thread's part) ...
         __syncthreads();  // ... and everyone's
+        const bool drawn = L.policy == kPolicyRandom;
+        const uint64_t stream = drawn ? splitmix64(L.seed, (uint64_t)b) : 0ull;
+        const uint64_t call = (uint64_t)(uint32_t)t << 16;
         uint32_t kmin = 0xffffffffu, kmax = 0u;
         {
             uint32_t c = cand_base;
@@ -369,7 +385,13 @@ struct Request {
                     const int s = (lo & ~31) + __ffs(bits) - 1;
                     bits &= bits - 1;
                     sa[c++] = (uint16_t)s;
-                    const uint32_t key = keys[s] + 1u;
+                    uint32_t key;
+                    if (drawn) {  // the draw replaces the stamp as the sort key
+                        key = (uint32_t)(splitmix64(stream, call + (uint64_t)s) >> 32);
+                        keys[s] = key - 1u;
+                    } else {
+                        key = keys[s] + 1u;
+                    }
                     kmin = min(kmin, key);
                     kmax = max(kmax, key);
                 }

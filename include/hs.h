@@ -200,6 +200,34 @@ int hs_clear_status(hs_ctx* ctx);
 /* hs_set_flags -- HS_FLAG_* bits for later calls (0 restores the default). */
 int hs_set_flags(hs_ctx* ctx, unsigned flags);
 
+/* replacement policies (hs_set_policy) */
+#define HS_POLICY_LRU 0    /* the method's: victims are the least recently used slots */
+#define HS_POLICY_FIFO 1   /* victims are the slots filled longest ago; a hit does not renew */
+#define HS_POLICY_RANDOM 2 /* victims are drawn at random among the slots not hit */
+
+/*
+ * hs_set_policy -- the replacement policy of the hs_resolve / hs_resolve_host /
+ * hs_resolve_profiled calls enqueued after it returns (the blog commentary's Fig. 3
+ * discussion: LRU against policies that do not exploit locality; the pages name none,
+ * so the two plainest are offered for comparison). Everything but the choice of
+ * victims is the same under every policy: hits, the ascending-position order of the
+ * misses, the pairing of the r-th miss with the r-th victim, the page-table update.
+ *   HS_POLICY_LRU     victims in ascending (last_use, slot); hits and fills stamp t
+ *   HS_POLICY_FIFO    victims in ascending (last_use, slot), but a hit keeps its
+ *                     stamp, which is therefore the call that filled the slot
+ *   HS_POLICY_RANDOM  victims in ascending (key, slot) among the slots not hit, where
+ *                     the key of slot s at call t of request b is the high 32 bits of
+ *                     SplitMix64 output number t * 2^16 + s of the generator seeded
+ *                     with SplitMix64 output number b of `seed` (Steele, Lea and Flood,
+ *                     2014: output n of seed x is mix(x + (n + 1) * 0x9E3779B97F4A7C15),
+ *                     mix being Stafford's 13th mixer); stamps are kept as under LRU
+ * The state kept so far carries over (stamps mean the last use under LRU and RANDOM
+ * and the fill call under FIFO from then on). Calls captured into a CUDA graph keep
+ * the policy they were captured with. hs_resolve_noalloc always uses LRU.
+ * Returns HS_OK or HS_ERR_INVALID (unknown policy).
+ */
+int hs_set_policy(hs_ctx* ctx, int policy, uint64_t seed);
+
 /* Number of kernels one hs_resolve call enqueues under the current flags. */
 int hs_kernels_per_call(hs_ctx* ctx);
 

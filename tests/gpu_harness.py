@@ -50,8 +50,10 @@ class GpuRun:
 
 
 def run_and_compare(w: tracegen.Workload, T: int, B: int | None = None, sample=None,
-                    checkpoints=None, layer: int = 0, run: GpuRun | None = None) -> dict:
-    """Run T steps on the GPU, then replay the sampled requests on the oracle.
+                    checkpoints=None, layer: int = 0, run: GpuRun | None = None,
+                    policy: int = 0, seed: int = 0) -> dict:
+    """Run T steps on the GPU, then replay the sampled requests on the oracle, both
+    under replacement `policy` (0 LRU, 1 FIFO, 2 RANDOM with `seed`).
 
     Returns summary stats (total misses per sampled request). Raises AssertionError on
     the first difference.
@@ -62,6 +64,7 @@ def run_and_compare(w: tracegen.Workload, T: int, B: int | None = None, sample=N
     sample = list(range(B)) if sample is None else list(sample)
     checkpoints = sorted(set(checkpoints or [T - 1]))
     snaps = {}
+    run.ctx.set_policy(policy, seed)
     for t in range(T):
         run.step(t)
         if t in checkpoints:
@@ -72,6 +75,8 @@ def run_and_compare(w: tracegen.Workload, T: int, B: int | None = None, sample=N
     miss = run.miss_dev[:, sample].cpu().numpy()
 
     o = Oracle(len(sample), w.C, w.S, w.E)
+    o.set_policy(policy, seed)
+    o.set_request_ids(sample)  # RANDOM's draws depend on the request number
     base = run.ctx.host_kv_address()
     row_bytes = w.C * run.ctx.host_stride
     for t in range(T):

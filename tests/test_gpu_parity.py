@@ -65,6 +65,53 @@ def test_quest_pages_eight_layers_reduced_batch():
         run.close()
 
 
+# ------------------------------------------------------------------ replacement policies
+
+@pytest.mark.parametrize("policy", [hs.POLICY_FIFO, hs.POLICY_RANDOM])
+def test_policy_dsa_full_trace_all_requests(policy):
+    w = tracegen.WORKLOADS["dsa"]
+    run_and_compare(w, T=64, checkpoints=[0, 1, 17, 63], policy=policy, seed=0x5EED)
+
+
+@pytest.mark.parametrize("policy", [hs.POLICY_FIFO, hs.POLICY_RANDOM])
+@pytest.mark.parametrize("C,S,k,E,B", [(37, 5, 5, 16, 3), (300, 33, 7, 48, 2), (100000, 777, 513, 144, 5)])
+def test_policy_ragged_shapes(policy, C, S, k, E, B):
+    w = tracegen.Workload("ragged", 9, B=B, L=1, C=C, S=S, k=k, E=E, kv_kind=tracegen.KV_RAW,
+                          T=40, keep_pct=60, zipf_s=1.1, seed=C)
+    run_and_compare(w, T=w.T, checkpoints=[0, 1, 19, 39], policy=policy, seed=C * 7919)
+
+
+def test_policy_random_sampled_requests_use_their_own_draws():
+    """Sampled requests (oracle rows standing for request numbers 3, 40, 63) draw the
+    keys of their own request numbers."""
+    w = tracegen.sweep_workload(4096, 80)
+    run_and_compare(w, T=24, sample=[3, 40, 63], checkpoints=[0, 23], policy=hs.POLICY_RANDOM, seed=1)
+
+
+def test_policy_switch_mid_trace():
+    """The state carries over when the policy changes between calls."""
+    w = tracegen.WORKLOADS["tiny"]
+    T = 30
+    run = GpuRun(w, T)
+    o = Oracle(run.B, w.C, w.S, w.E)
+    host = run.ctx.host_kv()
+    for t in range(T):
+        policy = (hs.POLICY_LRU, hs.POLICY_FIFO, hs.POLICY_RANDOM)[(t // 7) % 3]
+        run.ctx.set_policy(policy, 77)
+        o.set_policy(policy, 77)
+        run.step(t)
+        o_out, o_miss, _ = o.resolve(host, run.ctx.host_stride, run.sel[t])
+        assert np.array_equal(run.out_dev[t].cpu().numpy(), o_out), t
+        assert np.array_equal(run.miss_dev[t].cpu().numpy(), o_miss), t
+    torch.cuda.synchronize()
+    for name, ref in (("page_table", o.pt), ("slot_token", o.tok), ("last_use", o.lu), ("step", o.t)):
+        assert np.array_equal(getattr(run.ctx, name)().cpu().numpy(), ref), name
+    assert np.array_equal(run.ctx.device_kv().cpu().numpy(), o.dev)
+    with pytest.raises(RuntimeError):
+        run.ctx.set_policy(3)
+    run.close()
+
+
 # ------------------------------------------------------------------ properties and edge cases
 
 def test_noio_all_hits_after_first_call():
