@@ -75,6 +75,13 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.orc_splitmix64.restype = u64
         lib.orc_random_key.argtypes = [u64, i32, i32, i32]
         lib.orc_random_key.restype = ctypes.c_uint32
+        f64 = ctypes.c_double
+        lib.orc_e4m3.argtypes = [ctypes.c_uint8]
+        lib.orc_e4m3.restype = f64
+        lib.orc_bf16.argtypes = [ctypes.c_uint16]
+        lib.orc_bf16.restype = f64
+        lib.orc_attend.argtypes = [vp, i32, vp, i32, vp, i32, f64, vp, vp, vp]
+        lib.orc_attend.restype = i32
         _libs[path] = lib
     return lib
 
@@ -86,6 +93,11 @@ def _ptr(a: np.ndarray) -> int:
 def splitmix64(x: int, n: int) -> int:
     """SplitMix64 output number n of the generator seeded with x (the oracle's C)."""
     return int(load().orc_splitmix64(x & (2**64 - 1), n & (2**64 - 1)))
+
+
+def e4m3(code: int) -> float:
+    """Value of an OCP E4M3 code (the oracle's C)."""
+    return float(load().orc_e4m3(code))
 
 
 def random_key(seed: int, b: int, t: int, s: int) -> int:
@@ -184,6 +196,22 @@ class Oracle:
         if rc < 0:
             raise ValueError(f"orc_resolve_request failed ({rc})")
         return out, int(miss[0]), rc
+
+    def attend(self, b: int, q: np.ndarray, out_slots_b: np.ndarray, sm_scale: float):
+        """Sparse attention of request b over the slots out_slots_b [k] (negative = not
+        valid), q [H][576] as uint16 bf16 bit patterns. Returns (o [H][512], lse [H],
+        absw [H][512]) in float64."""
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        sl = np.ascontiguousarray(out_slots_b, dtype=np.int32)
+        H, k = q.shape[0], sl.shape[0]
+        out = np.empty((H, 512))
+        lse = np.empty(H)
+        absw = np.empty((H, 512))
+        rc = self._lib.orc_attend(self._h, b, _ptr(q), H, _ptr(sl), k, float(sm_scale), _ptr(out),
+                                  _ptr(lse), _ptr(absw))
+        if rc < 0:
+            raise ValueError(f"orc_attend failed ({rc})")
+        return out, lse, absw
 
     def append(self, host: np.ndarray, positions, rows: np.ndarray) -> int:
         """Decode-time append for all R requests: host [R][C][stride] (written), positions

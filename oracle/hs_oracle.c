@@ -51,8 +51,11 @@
  * bound k - floor(keep * k), and the invariants of an exact cache. The variants
  * are pinned by Belady's textbook string (FIFO and LRU fault counts), a textbook
  * FIFO queue, SplitMix64's published outputs with victims recomputed from them, the
- * uniformity of RANDOM's victims, and the loop of S + 1 positions.
+ * uniformity of RANDOM's victims, and the loop of S + 1 positions. The consumer is
+ * pinned by the E4M3 definition and PyTorch's decoder, library softmax attention on small
+ * cases, and closed forms (one entry, repeated entries, no valid entry, reordering).
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -285,3 +288,98 @@ int orc_append(orc_state* o, int b, uint8_t* host_b, size_t host_stride, int32_t
     return 0;
 }
 
+
+/*
+ * ---------------------------------------------------------------------------------
+ * The consumer: sparse attention over the resolved slots (the blog commentary, section
+ * two: a resident entry takes part in the layer's computation directly; paper
+ * abstract: only placement changes, so the consumer's outputs are unchanged).
+ *
+ * The pages fix no attention arithmetic; this is the plainest reading for the 656-byte
+ * DSA-style entries of the DeepSeek sparse-attention family the pages evaluate, an
+ * MLA decode in its absorbed form:
+ *   entry bytes [0, 512)    e4m3 codes c_0..c_511 of the latent vector
+ *               [512, 528)  four fp32 scales; scale g applies to codes 128g..128g+127
+ *               [528, 656)  64 bf16 values of the rotary part
+ *   key   K_j = (c_j * scale, rope_j)  in R^576,   value  V_j = c_j * scale  in R^512;
+ *   for head h with query q_h in R^576 (bf16) and the selections j whose slot is >= 0:
+ *   s_hj = sm_scale * <q_h, K_j>,  o_h = sum_j softmax_j(s_h) V_j,  lse_h = ln sum_j exp(s_hj).
+ * A head with no valid selection gets o_h = 0 and lse_h = -inf. All arithmetic is fp64.
+ * e4m3 is the OCP 8-bit floating point format E4M3: sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits, subnormals at exponent 0, no infinities, S.1111.111 is NaN.
+ */
+double orc_e4m3(uint8_t c) {
+    const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+double orc_bf16(uint16_t h) {
+    const uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/*
+ * Attention of request b over its selections: out_b[k] are the slots hs resolution
+ * returned (negative = not a valid selection), q [H][576] bf16 bit patterns. Writes
+ * o [H][512], lse [H], and absw [H][512] = sum_j softmax_j |V_j| (the scale of the
+ * values each output averages, for error bounds). Needs E == 656.
+ */
+int orc_attend(const orc_state* o, int b, const uint16_t* q, int H, const int32_t* out_b, int k,
+               double sm_scale, double* out, double* lse, double* absw) {
+    if (!o || b < 0 || b >= o->R || o->E != 656 || !q || H <= 0 || !out_b || k <= 0 || !out || !lse || !absw)
+        return ORC_EINVAL;
+    const int S = o->S;
+    double* K = (double*)malloc(sizeof(double) * (size_t)k * 576);
+    double* s = (double*)malloc(sizeof(double) * (size_t)k);
+    int* use = (int*)malloc(sizeof(int) * (size_t)k);
+    if (!K || !s || !use) { free(K); free(s); free(use); return ORC_ENOMEM; }
+    for (int j = 0; j < k; ++j) {
+        const int32_t sl = out_b[j];
+        use[j] = sl >= 0 && sl < S;
+        if (!use[j]) continue;
+        const uint8_t* row = o->dev + ((size_t)b * S + sl) * 656;
+        for (int d = 0; d < 512; ++d) {
+            float sc;
+            memcpy(&sc, row + 512 + 4 * (d / 128), 4);
+            K[(size_t)j * 576 + d] = orc_e4m3(row[d]) * (double)sc;
+        }
+        for (int d = 0; d < 64; ++d) {
+            uint16_t h;
+            memcpy(&h, row + 528 + 2 * d, 2);
+            K[(size_t)j * 576 + 512 + d] = orc_bf16(h);
+        }
+    }
+    for (int h = 0; h < H; ++h) {
+        double mx = -INFINITY;
+        for (int j = 0; j < k; ++j) {
+            if (!use[j]) continue;
+            double acc = 0.0;
+            for (int d = 0; d < 576; ++d) acc += orc_bf16(q[(size_t)h * 576 + d]) * K[(size_t)j * 576 + d];
+            s[j] = sm_scale * acc;
+            if (s[j] > mx) mx = s[j];
+        }
+        double* oh = out + (size_t)h * 512;
+        double* wh = absw + (size_t)h * 512;
+        for (int d = 0; d < 512; ++d) { oh[d] = 0.0; wh[d] = 0.0; }
+        if (mx == -INFINITY) { lse[h] = -INFINITY; continue; }
+        double l = 0.0;
+        for (int j = 0; j < k; ++j) if (use[j]) l += exp(s[j] - mx);
+        for (int j = 0; j < k; ++j) {
+            if (!use[j]) continue;
+            const double w = exp(s[j] - mx) / l;
+            for (int d = 0; d < 512; ++d) {
+                oh[d] += w * K[(size_t)j * 576 + d];
+                wh[d] += w * fabs(K[(size_t)j * 576 + d]);
+            }
+        }
+        lse[h] = mx + log(l);
+    }
+    free(K); free(s); free(use);
+    return 0;
+}

@@ -8,6 +8,7 @@ import os
 
 import pytest
 
+from tests import test_oracle_attend as attend_pins
 from tests import test_oracle_pins as pins
 
 MUTANTS = {
@@ -26,6 +27,12 @@ MUTANTS = {
     "append_skips_resident_slot": ("if (s >= 0) memcpy(o->dev + ((size_t)b * o->S + s) * o->E, row, (size_t)o->E);", ""),
     "most_recent_first_order": ("if (x->key != y->key) return (x->key > y->key) - (x->key < y->key);",
                                 "if (x->key != y->key) return (x->key < y->key) - (x->key > y->key);"),
+    "attend_scale_block_of_64": ("memcpy(&sc, row + 512 + 4 * (d / 128), 4);", "memcpy(&sc, row + 512 + 4 * ((d / 64) & 3), 4);"),
+    "attend_rope_dropped": ("K[(size_t)j * 576 + 512 + d] = orc_bf16(h);", "K[(size_t)j * 576 + 512 + d] = 0.0;"),
+    "attend_lse_without_max": ("lse[h] = mx + log(l);", "lse[h] = log(l);"),
+    "attend_padding_clamped": ("const int32_t sl = out_b[j];", "const int32_t sl = out_b[j] < 0 ? 0 : out_b[j];"),
+    "e4m3_bias_8": ("else v = ldexp(1.0 + (double)m / 8.0, e - 7);", "else v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    "e4m3_subnormal_scale": ("if (e == 0) v = ldexp((double)m / 8.0, -6);", "if (e == 0) v = ldexp((double)m / 8.0, -7);"),
     "fifo_restamps_hits": ("if (o->policy != ORC_POLICY_FIFO)\n", "if (1)\n"),
     "random_key_low_bits": ("+ (uint64_t)s) >> 32);", "+ (uint64_t)s));"),
     "random_key_ignores_request": ("orc_random_key(o->seed, o->rid[b], t, s)", "orc_random_key(o->seed, b, t, s)"),
@@ -35,6 +42,7 @@ MUTANTS = {
 
 
 def _pin_suite(Oracle, path):
+    attend_pins.run_attend(Oracle, path)
     pins.run_policies(Oracle, path)
     pins.run_append(Oracle, path)
     pins.run_hand_trace(Oracle, path)
