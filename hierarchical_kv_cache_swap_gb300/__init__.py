@@ -53,6 +53,8 @@ SIGNATURES = {
     "hs_clear_status": (_I, [_VP]),
     "hs_set_flags": (_I, [_VP, _U]),
     "hs_set_policy": (_I, [_VP, _I, ctypes.c_uint64]),
+    "hs_attend": (_I, [_VP, _VP, _VP, _I, _I, _VP, _I, ctypes.c_float, _VP, _VP, _VP, ctypes.c_size_t]),
+    "hs_attend_workspace": (_I, [_VP, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
     "hs_kernels_per_call": (_I, [_VP]),
     "hs_last_error": (ctypes.c_char_p, []),
     "hs_resolve_noalloc": (_I, [_VP, _I, _I, _I, _I, _VP, _SZ, _VP, _VP, _VP, _VP, _VP, _VP, _I,
@@ -203,6 +205,22 @@ class Context:
         no new entry) into the host store (and resident slots)."""
         self._check(self._lib.hs_append(self._h, _stream(stream), _addr(kv), _addr(positions),
                                         positions.shape[0]), "hs_append")
+
+    def attend_workspace(self, B: int, H: int, k: int) -> int:
+        """Bytes of device scratch hs_attend needs for (B, H, k)."""
+        n = ctypes.c_size_t(0)
+        self._check(self._lib.hs_attend_workspace(self._h, B, H, k, ctypes.byref(n)), "hs_attend_workspace")
+        return int(n.value)
+
+    def attend(self, q, out_slots, o, lse, sm_scale: float, workspace=None, stream=None) -> None:
+        """Sparse attention over the resolved slots: q bf16 [R, H, 576], out_slots int32
+        [R, k], o float32 [R, H, 512] and lse float32 [R, H] (device); workspace: a device
+        buffer of attend_workspace() bytes (None when that is 0)."""
+        B, H, _ = q.shape
+        k = out_slots.shape[1]
+        ws, nbytes = (None, 0) if workspace is None else (_addr(workspace), workspace.numel() * workspace.element_size())
+        self._check(self._lib.hs_attend(self._h, _stream(stream), _addr(q), B, H, _addr(out_slots), k,
+                                        float(sm_scale), _addr(o), _addr(lse), ws, nbytes), "hs_attend")
 
     def reset(self, stream=None) -> None:
         self._check(self._lib.hs_reset(self._h, _stream(stream)), "hs_reset")

@@ -27,6 +27,7 @@ struct hs_ctx {
     int32_t* stage_sel;    // [R][S] staging for hs_resolve_host
     int32_t* stage_out;    // [R][S]
     int32_t* stage_miss;   // [R]
+    bool attend_ok;        // the attention kernel's shared memory fits this device
 };
 
 namespace {
@@ -207,6 +208,12 @@ hs_ctx* create(int num_requests, int context_len, int slots, int entry_bytes, ui
         free_ctx(h);
         return nullptr;
     }
+    {  // the attention consumer needs one SM's worth of shared memory
+        int optin = 0;
+        h->attend_ok = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+                       (size_t)optin >= hs::attend_smem_bytes() && hs::configure_attend() == cudaSuccess;
+        cudaGetLastError();
+    }
     if (hs_reset(h, nullptr) != HS_OK) {
         free_ctx(h);
         return nullptr;
@@ -246,6 +253,43 @@ int hs_append(hs_ctx* h, hs_stream_t stream, const uint8_t* kv, const int32_t* p
     if (B > 65535) return fail(HS_ERR_LIMIT, "hs_append handles at most 65535 requests");
     cudaError_t e = hs::launch_append(h->L, (cudaStream_t)stream, kv, positions);
     if (e != cudaSuccess) return cuda_fail(e, "append kernel launch");
+    g_err[0] = 0;
+    return HS_OK;
+}
+
+static int attend_check(hs_ctx* h, int B, int H, int k) {
+    if (!h) return fail(HS_ERR_INVALID, "null context");
+    if (h->L.E != hs::kAttendEntryBytes)
+        return fail(HS_ERR_INVALID, "hs_attend needs %d-byte entries, the context has %d", hs::kAttendEntryBytes, h->L.E);
+    if (B != h->L.R) return fail(HS_ERR_INVALID, "B=%d but the context has %d requests", B, h->L.R);
+    if (H < 1 || H > hs::kAttendMaxHeads) return fail(HS_ERR_INVALID, "H=%d must be in [1, %d]", H, hs::kAttendMaxHeads);
+    if (k < 1) return fail(HS_ERR_INVALID, "k=%d must be >= 1", k);
+    if (!h->attend_ok) return fail(HS_ERR_INVALID, "the device cannot hold the attention kernel's shared memory");
+    return HS_OK;
+}
+
+int hs_attend_workspace(hs_ctx* h, int B, int H, int k, size_t* bytes) {
+    int rc = attend_check(h, B, H, k);
+    if (rc != HS_OK) return rc;
+    if (!bytes) return fail(HS_ERR_INVALID, "null bytes");
+    *bytes = hs::attend_plan(B, H, k, h->num_sms).workspace_bytes;
+    g_err[0] = 0;
+    return HS_OK;
+}
+
+int hs_attend(hs_ctx* h, hs_stream_t stream, const void* q, int B, int H, const int32_t* out_slots, int k,
+              float sm_scale, float* o, float* lse, void* workspace, size_t workspace_bytes) {
+    int rc = attend_check(h, B, H, k);
+    if (rc != HS_OK) return rc;
+    if (!q || !out_slots || !o || !lse) return fail(HS_ERR_INVALID, "null q/out_slots/o/lse");
+    if (((uintptr_t)q & 15) || ((uintptr_t)o & 15)) return fail(HS_ERR_INVALID, "q and o must be 16-byte aligned");
+    const hs::AttendPlan plan = hs::attend_plan(B, H, k, h->num_sms);
+    if (plan.workspace_bytes > 0 && (!workspace || workspace_bytes < plan.workspace_bytes || ((uintptr_t)workspace & 15)))
+        return fail(HS_ERR_INVALID, "workspace of %zu bytes (16-byte aligned) needed, %zu given", plan.workspace_bytes,
+                    workspace_bytes);
+    cudaError_t e = hs::launch_attend(h->L, (cudaStream_t)stream, (const uint16_t*)q, B, H, out_slots, k, sm_scale, o,
+                                      lse, workspace, plan);
+    if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
     g_err[0] = 0;
     return HS_OK;
 }

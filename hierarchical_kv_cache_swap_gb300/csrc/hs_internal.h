@@ -86,6 +86,21 @@ cudaError_t launch_checksum(const uint8_t* dev, int R, int S, int E, const int32
 // Enqueue the decode-time append of kv[b] (device [R][E]) at positions[b] (device [R]).
 cudaError_t launch_append(const Layout& L, cudaStream_t stream, const uint8_t* kv, const int32_t* positions);
 
+// Sparse MLA-style decode attention over resolved slots (hs_attend.cu).
+struct AttendPlan {
+    int nsplit = 1;              // key splits per request
+    int keys_per_split = 0;      // a multiple of the 32-key stage
+    size_t workspace_bytes = 0;  // partial outputs when nsplit > 1
+};
+constexpr int kAttendEntryBytes = 656;
+constexpr int kAttendMaxHeads = 128;
+size_t attend_smem_bytes();
+AttendPlan attend_plan(int B, int H, int k, int num_sms);
+cudaError_t configure_attend();
+cudaError_t launch_attend(const Layout& L, cudaStream_t stream, const uint16_t* q, int B, int H,
+                          const int32_t* out_slots, int k, float sm_scale, float* o, float* lse,
+                          void* workspace, const AttendPlan& plan);
+
 // Set the calling thread's message for hs_last_error().
 void record_error(const char* msg);
 

@@ -154,6 +154,34 @@ int hs_resolve_profiled(hs_ctx* ctx, hs_stream_t stream, const int32_t* selectio
 int hs_append(hs_ctx* ctx, hs_stream_t stream, const uint8_t* kv, const int32_t* positions, int B);
 
 /*
+ * hs_attend -- the layer's consumer: sparse attention of every request over the slots
+ * its selections resolved to (blog commentary, section two: a resident entry takes part
+ * in the computation directly; paper abstract: only placement changes, so outputs are
+ * unchanged). For the 656-byte entries of the DeepSeek sparse-attention family (the
+ * context's entry_bytes must be 656): bytes [0,512) are E4M3 codes of the latent vector,
+ * [512,528) four fp32 scales (scale g for codes 128g..128g+127), [528,656) 64 bf16 rotary
+ * values. Key K_j = (latent_j * scale, rope_j) in R^576, value V_j = latent_j * scale in
+ * R^512; for head h and the selections j with out_slots[b][j] >= 0:
+ *   s_hj = sm_scale * <q_h, K_j>,  o[b][h] = sum_j softmax_j(s_h) V_j,  lse[b][h] = ln sum_j exp(s_hj).
+ * A head with no valid selection gets o = 0 and lse = -inf.
+ *   q          device bf16 [B][H][576], 16-byte aligned
+ *   out_slots  device int32 [B][k] as written by hs_resolve (negative = not valid)
+ *   o, lse     device fp32 [B][H][512] (16-byte aligned) and [B][H], overwritten
+ *   workspace  device scratch of hs_attend_workspace() bytes (may be NULL when that is 0)
+ * The latent codes are decoded to bf16 (code * scale rounded to nearest even), the
+ * products run on the tensor cores with fp32 accumulation, and the softmax weights are
+ * rounded to bf16 before the value product. B must equal num_requests, 1 <= H <= 128,
+ * k >= 1. Enqueue-only: no allocation, no host synchronisation, graph-capturable. A
+ * stalled pipeline sets HS_STATUS_TIMEOUT. Returns HS_OK, HS_ERR_INVALID or HS_ERR_CUDA.
+ */
+int hs_attend(hs_ctx* ctx, hs_stream_t stream, const void* q, int B, int H, const int32_t* out_slots, int k,
+              float sm_scale, float* o, float* lse, void* workspace, size_t workspace_bytes);
+
+/* hs_attend_workspace -- *bytes = the workspace hs_attend needs for (B, H, k) on this
+ * context's device (0 when a request's keys fit one pass). Returns HS_OK or HS_ERR_INVALID. */
+int hs_attend_workspace(hs_ctx* ctx, int B, int H, int k, size_t* bytes);
+
+/*
  * hs_checksum_rows -- a stand-in for the sparse-attention consumer of a layer (blog
  * commentary, section two: a resident entry takes part in the computation directly).
  * Enqueues on `stream` a kernel that reads the k rows each request resolved to, through
