@@ -46,30 +46,37 @@ constexpr int kHeads = 128;    // MMA rows
 constexpr int kDimK = 576;     // 512 latent + 64 rotary
 constexpr int kDimV = 512;
 constexpr int kHalfV = 256;    // value dimensions per CTA
-constexpr int kBlk = 32;       // keys per stage
+constexpr int kBlk = 256;      // keys per block: the N of S = Q K^T
 constexpr int kChunks = kDimK / 64;                  // 64-element (128-byte) swizzle columns
 constexpr uint32_t kQChunk = kHeads * 128;           // bytes of one Q column chunk
-constexpr uint32_t kKChunk = kBlk * 128;             // bytes of one stage column chunk
 constexpr uint32_t kQBytes = kQChunk * kChunks;      // 147456
-constexpr uint32_t kStageBytes = kKChunk * kChunks;  // 36864
-constexpr int kSoftWarps = 4, kProdWarps = 8;
-constexpr int kThreads = (kSoftWarps + kProdWarps + 1) * 32;  // 416
+constexpr uint32_t kStageBytes = 32768;              // K chunk: 256 keys x 64 dims; V chunk: 64 keys x 256 dims
+constexpr int kStages = 2;
+constexpr int kKFills = kChunks;                     // K chunks per block (8 latent + 1 rotary)
+constexpr int kVKeys = 64;                           // keys per V chunk
+constexpr int kVFills = kBlk / kVKeys;               // V chunks per block
+constexpr int kFills = kKFills + kVFills;            // stage fills per block
+constexpr uint32_t kVSub = kVKeys * 128;             // bytes of one 64-dimension column of a V chunk
+constexpr int kSoftWarps = 4, kProdWarps = 16;
+constexpr int kThreads = (kSoftWarps + kProdWarps + 1) * 32;  // 672
 constexpr int kMmaWarp = kSoftWarps + kProdWarps;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 256, kColP = 320;  // S[st] at 256+32st, P[st] at 320+16st
+constexpr uint32_t kColO = 0, kColS = 256;  // O: 256 columns; S: 256 columns, P (bf16) written over its first 128
 constexpr float kRescaleLog2 = 8.0f;
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls of an mbarrier before giving up
+constexpr int kMaxSplitKeys = 2048;        // slots of one split staged in shared memory
 
 // barrier indices
-enum { kQFull = 0, kKvFull = 1, kKvFree = 3, kSFull = 5, kPFull = 7, kPvDone = 9, kOFull = 11, kDrain = 12, kBars = 13 };
+enum { kQFull = 0, kFull = 1, kFree = 3, kSFull = 5, kPFull = 6, kPvDone = 7, kVmFull = 8, kDrain = 10, kBars = 11 };
 
-struct Smem {  // beyond Q and the two stages
+struct Smem {  // beyond Q and the stages
+    int32_t slot[kMaxSplitKeys];  // this split's out_slots
     uint64_t bar[kBars];
-    uint32_t vmask[2];  // valid keys of each stage
+    uint32_t vmask[2][kBlk / 32];  // valid keys of a block, by block parity
     uint32_t tmem;
     volatile int abort;
 };
-constexpr uint32_t kSmemBytes = 1024 + kQBytes + 2 * kStageBytes + sizeof(Smem);
+constexpr uint32_t kSmemBytes = 1024 + kQBytes + kStages * kStageBytes + sizeof(Smem);
 
 struct AttendArgs {
     const uint8_t* dev;        // [R][S][656]
@@ -210,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = base;
     uint8_t* sK = base + kQBytes;  // stage st at sK + st * kStageBytes
-    Smem* sm = reinterpret_cast<Smem*>(base + kQBytes + 2 * kStageBytes);
+    Smem* sm = reinterpret_cast<Smem*>(base + kQBytes + kStages * kStageBytes);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int v = blockIdx.x & 1;
     const int split = (blockIdx.x >> 1) % A.nsplit;
@@ -221,14 +228,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
 
     if (tid == 0) {
         bar_init(&sm->bar[kQFull], kProdWarps * 32);
-        for (int st = 0; st < 2; ++st) {
-            bar_init(&sm->bar[kKvFull + st], kProdWarps * 32);
-            bar_init(&sm->bar[kKvFree + st], 1);
-            bar_init(&sm->bar[kSFull + st], 1);
-            bar_init(&sm->bar[kPFull + st], kSoftWarps * 32);
-            bar_init(&sm->bar[kPvDone + st], 1);
+        for (int st = 0; st < kStages; ++st) {
+            bar_init(&sm->bar[kFull + st], kProdWarps * 32);
+            bar_init(&sm->bar[kFree + st], 1);
+            bar_init(&sm->bar[kVmFull + st], kBlk / 32);
         }
-        bar_init(&sm->bar[kOFull], 1);
+        bar_init(&sm->bar[kSFull], 1);
+        bar_init(&sm->bar[kPFull], kSoftWarps * 32);
+        bar_init(&sm->bar[kPvDone], 1);
         bar_init(&sm->bar[kDrain], 1);
         sm->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -245,53 +252,132 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
 
     if (warp >= kSoftWarps && warp < kMmaWarp) {
         // ------------------------------------------------------------ producers
-        const int pw = warp - kSoftWarps;  // the 64-dimension slice (and rotary unit) of this warp
-        const int ptid = tid - kSoftWarps * 32;
-        {  // Q, once: rows h < H of request b, zero rows beyond
-            const uint4* qb = reinterpret_cast<const uint4*>(A.q + (size_t)b * A.H * kDimK);
+        const int pw = warp - kSoftWarps;
+        const int ptid = tid - kSoftWarps * 32;  // 0..255
+        {  // Q, once, by asynchronous copies (rows h >= H are zero-filled)
+            const uint8_t* qb = reinterpret_cast<const uint8_t*>(A.q + (size_t)b * A.H * kDimK);
             for (int u = ptid; u < kHeads * (kDimK / 8); u += kProdWarps * 32) {
                 const int h = u / (kDimK / 8), cu = u - h * (kDimK / 8);
-                const uint4 val = h < A.H ? __ldg(qb + (size_t)h * (kDimK / 8) + cu) : make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(sQ + (cu >> 3) * kQChunk + swz(h, cu & 7)) = val;
+                const uint32_t dst = su32(sQ + (cu >> 3) * kQChunk + swz(h, cu & 7));
+                const uint8_t* src = qb + ((size_t)min(h, A.H - 1) * (kDimK / 8) + cu) * 16;
+                const uint32_t n = h < A.H ? 16u : 0u;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            bar_arrive(&sm->bar[kQFull]);
+            asm volatile("cp.async.commit_group;" ::: "memory");
         }
+        // the split's slots, staged once
         const int32_t* slots = A.out_slots + (size_t)b * A.k;
-        for (int i = 0; i < nb; ++i) {
-            const int st = i & 1;
-            const int j = kbeg + i * kBlk + lane;
-            int32_t s = j < kend ? __ldg(slots + j) : -1;
-            const bool valid = s >= 0 && s < A.S;
-            uint4 c[4];
-            uint4 rope = make_uint4(0, 0, 0, 0);
-            float scale = 0.f;
-            if (valid) {
-                const uint8_t* row = A.dev + ((size_t)b * A.S + s) * 656;
-                const uint4* cr = reinterpret_cast<const uint4*>(row + 64 * pw);
+        for (int j = ptid; j < kend - kbeg; j += kProdWarps * 32) sm->slot[j] = __ldg(slots + kbeg + j);
+        asm volatile("bar.sync 1, %0;" ::"r"(kProdWarps * 32) : "memory");
+        auto slot_at = [&](int j) -> int32_t {  // key j of the split; -1 when past its end or invalid
+            const int32_t s = kbeg + j < kend ? sm->slot[j] : -1;
+            return (s >= 0 && s < A.S) ? s : -1;
+        };
+        auto row_of = [&](int32_t s) { return A.dev + ((size_t)b * A.S + s) * 656; };
+        auto prefetch_block = [&](int i) {  // this warp's 32 rows of the block into L2
+            if (i >= nb || ptid >= kBlk) return;
+            const int32_t s = slot_at(i * kBlk + ptid);
+            if (s >= 0) asm volatile("cp.async.bulk.prefetch.L2.global [%0], 656;" ::"l"(row_of(s)) : "memory");
+        };
+        prefetch_block(0);
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        bar_arrive(&sm->bar[kQFull]);
+        // Stage fills, in the order the MMAs consume them: per block the 9 K chunks (8
+        // latent, then the rotary one) and the 4 V chunks. Loads are spread so that the
+        // lanes of a warp read a few whole stretches of a row each (4 lanes x 16 bytes
+        // per key for a K chunk, 16 lanes for a V chunk, 8 lanes for the rotary chunk):
+        // a warp-wide load then touches 8 (or 2, or 4) rows rather than 32. The raw bytes
+        // of fill g + 2 are requested before fill g is decoded; three register buffers
+        // rotate by unrolling, so two fills' loads are always in flight.
+        constexpr int kW = 1024 / (kProdWarps * 32);  // (key, 16-byte unit) items per thread in a K or V chunk
+        struct Raw {
+            uint4 c[kW];
+            float scale[kW];
+        };
+        const int total = nb * kFills;
+        const int kq = ptid & 3, kkey = ptid >> 2;    // K chunk: quarter of the 64 dims, key (+128 w)
+        const int vu = ptid & 15, vkey = ptid >> 4;   // V chunk: 16-dim unit of the half, key (+32 w)
+        const int rq = ptid & 7, rkey = ptid >> 3;    // rotary chunk: 16-byte unit, key (+64 w)
+        auto issue = [&](int g, Raw& r) {
+            if (g >= total) return;
+            const int i = g / kFills, f = g - i * kFills;
+            if (f == kKFills - 1) return;  // the rotary chunk is copied asynchronously
 #pragma unroll
-                for (int q = 0; q < 4; ++q) c[q] = __ldg(cr + q);
-                scale = __ldg(reinterpret_cast<const float*>(row + 512) + (pw >> 1));
-                rope = __ldg(reinterpret_cast<const uint4*>(row + 528) + pw);
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) c[q] = make_uint4(0, 0, 0, 0);
+            for (int w = 0; w < kW; ++w) {
+                int32_t s;
+                int off;
+                if (f < kKFills) {
+                    s = slot_at(i * kBlk + kkey + 128 * w);
+                    off = 64 * f + 16 * kq;
+                } else {
+                    s = slot_at(i * kBlk + (f - kKFills) * kVKeys + vkey + 32 * w);
+                    off = kHalfV * v + 16 * vu;
+                }
+                if (s >= 0) {
+                    const uint8_t* row = row_of(s);
+                    r.c[w] = __ldg(reinterpret_cast<const uint4*>(row + off));
+                    r.scale[w] = __ldg(reinterpret_cast<const float*>(row + 512) + (off >> 7));
+                } else {
+                    r.c[w] = make_uint4(0, 0, 0, 0);
+                    r.scale[w] = 0.f;
+                }
             }
-            if (i >= 2 && !bar_wait(sm, &sm->bar[kKvFree + st], ((i >> 1) & 1) ^ 1, A.status)) break;
+        };
+        auto process = [&](int g, const Raw& r) -> bool {
+            const int i = g / kFills, f = g - i * kFills;
+            if (f == 0 && pw < kBlk / 32) {  // a new block: its valid keys (32 per warp)
+                const uint32_t m = __ballot_sync(0xffffffffu, slot_at(i * kBlk + ptid) >= 0);
+                if (lane == 0) {
+                    sm->vmask[i & 1][pw] = m;
+                    bar_arrive(&sm->bar[kVmFull + (i & 1)]);
+                }
+            }
+            if (pw < kBlk / 32 && f == pw) prefetch_block(i + 1);  // the next block's rows into L2
+            const int st = g & 1;
+            if (g >= 2 && !bar_wait(sm, &sm->bar[kFree + st], ((g >> 1) & 1) ^ 1, A.status)) return false;
             uint8_t* stg = sK + st * kStageBytes;
-            uint8_t* col = stg + pw * kKChunk;
+            if (f == kKFills - 1) {  // rotary values: bf16 already, copied as they are
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                *reinterpret_cast<uint4*>(col + swz(lane, 2 * q)) = decode8(c[q].x, c[q].y, scale);
-                *reinterpret_cast<uint4*>(col + swz(lane, 2 * q + 1)) = decode8(c[q].z, c[q].w, scale);
-            }
-            *reinterpret_cast<uint4*>(stg + 8 * kKChunk + swz(lane, pw)) = rope;
-            if (pw == 0) {
-                const uint32_t m = __ballot_sync(0xffffffffu, valid);
-                if (lane == 0) sm->vmask[st] = m;
+                for (int w = 0; w < 2 * kW; ++w) {
+                    const int key = rkey + 64 * w;
+                    const int32_t s = slot_at(i * kBlk + key);
+                    const uint8_t* src = row_of(s >= 0 ? s : 0) + 528 + 16 * rq;
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(su32(stg + swz(key, rq))),
+                                 "l"(src), "r"(s >= 0 ? 16u : 0u) : "memory");
+                }
+                asm volatile("cp.async.commit_group;" ::: "memory");
+                asm volatile("cp.async.wait_all;" ::: "memory");
+            } else if (f < kKFills) {
+#pragma unroll
+                for (int w = 0; w < kW; ++w) {
+                    const int key = kkey + 128 * w;
+                    *reinterpret_cast<uint4*>(stg + swz(key, 2 * kq)) = decode8(r.c[w].x, r.c[w].y, r.scale[w]);
+                    *reinterpret_cast<uint4*>(stg + swz(key, 2 * kq + 1)) = decode8(r.c[w].z, r.c[w].w, r.scale[w]);
+                }
+            } else {
+                uint8_t* col = stg + (vu >> 2) * kVSub;  // the 64-dim column of this unit
+#pragma unroll
+                for (int w = 0; w < kW; ++w) {
+                    const int key = vkey + 32 * w;
+                    *reinterpret_cast<uint4*>(col + swz(key, 2 * (vu & 3))) = decode8(r.c[w].x, r.c[w].y, r.scale[w]);
+                    *reinterpret_cast<uint4*>(col + swz(key, 2 * (vu & 3) + 1)) = decode8(r.c[w].z, r.c[w].w, r.scale[w]);
+                }
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            bar_arrive(&sm->bar[kKvFull + st]);
+            bar_arrive(&sm->bar[kFull + st]);
+            return true;
+        };
+        Raw r0, r1, r2;
+        issue(0, r0);
+        issue(1, r1);
+        for (int g = 0; g < total; g += 3) {
+            issue(g + 2, r2);
+            if (!process(g, r0) || g + 1 >= total) break;
+            issue(g + 3, r0);
+            if (!process(g + 1, r1) || g + 2 >= total) break;
+            issue(g + 4, r1);
+            if (!process(g + 2, r2)) break;
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issue (one thread)
@@ -300,35 +386,39 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
             const uint32_t id_o = idesc_bf16(kHeads, kHalfV, 1);
             const uint32_t q0 = su32(sQ), k0 = su32(sK);
             bool ok = bar_wait(sm, &sm->bar[kQFull], 0, A.status);
-            auto do_pv = [&](int ib) -> bool {
-                const int st = ib & 1;
-                if (!bar_wait(sm, &sm->bar[kPFull + st], (ib >> 1) & 1, A.status)) return false;
-                fence_after();
-                const uint32_t vb = k0 + st * kStageBytes + (uint32_t)(4 * v) * kKChunk;
-#pragma unroll
-                for (int ks = 0; ks < kBlk / 16; ++ks)
-                    mma_ts(tmem + kColO, tmem + kColP + 16 * st + 8 * ks,
-                           smem_desc(vb + ks * 2048, kKChunk, 1024), id_o, (ib > 0 || ks > 0) ? 1u : 0u);
-                mma_commit(&sm->bar[kKvFree + st]);
-                mma_commit(&sm->bar[kPvDone + st]);
-                return true;
-            };
+            uint32_t g = 0;
             for (int i = 0; ok && i < nb; ++i) {
-                const int st = i & 1;
-                if (!bar_wait(sm, &sm->bar[kKvFull + st], (i >> 1) & 1, A.status)) { ok = false; break; }
-                fence_after();
-                const uint32_t kb = k0 + st * kStageBytes;
-#pragma unroll 4
-                for (int kk = 0; kk < kDimK / 16; ++kk) {
-                    const uint32_t c = kk >> 2, w = (kk & 3) * 32;
-                    mma_ss(tmem + kColS + 32 * st, smem_desc(q0 + c * kQChunk + w, 16, 1024),
-                           smem_desc(kb + c * kKChunk + w, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+                // S and P share columns: block i's scores wait until block i-1's product is done
+                if (i > 0 && !bar_wait(sm, &sm->bar[kPvDone], (i - 1) & 1, A.status)) { ok = false; break; }
+                for (int c = 0; c < kKFills; ++c, ++g) {
+                    const int st = g & 1;
+                    if (!bar_wait(sm, &sm->bar[kFull + st], (g >> 1) & 1, A.status)) { ok = false; break; }
+                    fence_after();
+                    const uint32_t kb = k0 + st * kStageBytes;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss(tmem + kColS, smem_desc(q0 + c * kQChunk + kk * 32, 16, 1024),
+                               smem_desc(kb + kk * 32, 16, 1024), id_s, (c | kk) ? 1u : 0u);
+                    mma_commit(&sm->bar[kFree + st]);
                 }
-                mma_commit(&sm->bar[kSFull + st]);
-                if (i > 0 && !do_pv(i - 1)) { ok = false; break; }
+                if (!ok) break;
+                mma_commit(&sm->bar[kSFull]);
+                if (!bar_wait(sm, &sm->bar[kPFull], i & 1, A.status)) { ok = false; break; }
+                fence_after();
+                for (int vc = 0; vc < kVFills; ++vc, ++g) {
+                    const int st = g & 1;
+                    if (!bar_wait(sm, &sm->bar[kFull + st], (g >> 1) & 1, A.status)) { ok = false; break; }
+                    fence_after();
+                    const uint32_t vb = k0 + st * kStageBytes;
+#pragma unroll
+                    for (int ks = 0; ks < kVKeys / 16; ++ks)
+                        mma_ts(tmem + kColO, tmem + kColS + (kVKeys / 2) * vc + 8 * ks,
+                               smem_desc(vb + ks * 2048, kVSub, 1024), id_o, (i > 0 || vc > 0 || ks > 0) ? 1u : 0u);
+                    mma_commit(&sm->bar[kFree + st]);
+                }
+                if (!ok) break;
+                mma_commit(&sm->bar[kPvDone]);
             }
-            if (ok && nb > 0) ok = do_pv(nb - 1);
-            if (ok) mma_commit(&sm->bar[kOFull]);
             // whatever happened, every MMA issued here completes before the columns are freed
             mma_commit(&sm->bar[kDrain]);
             for (uint32_t it = 0; it < kWaitLimit && !bar_try(&sm->bar[kDrain], 0); ++it) {
@@ -342,26 +432,27 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int i = 0; i < nb; ++i) {
-            const int st = i & 1, ph = (i >> 1) & 1;
-            if (!warp_wait(sm, &sm->bar[kSFull + st], ph, A.status) ||
-                !warp_wait(sm, &sm->bar[kKvFull + st], ph, A.status)) { ok = false; break; }
+            if (!warp_wait(sm, &sm->bar[kSFull], i & 1, A.status) ||
+                !warp_wait(sm, &sm->bar[kVmFull + (i & 1)], (i >> 1) & 1, A.status)) { ok = false; break; }
             fence_after();
-            uint32_t r[32];
-            HS_LD32(r, tmem + lrow + kColS + 32 * st);
-            tmem_wait_ld();
-            const uint32_t vm = sm->vmask[st];
-            float x[32];
+            // pass 1: the block's maximum
             float mb = -INFINITY;
+#pragma unroll 1
+            for (int ch = 0; ch < kBlk / 32; ++ch) {
+                uint32_t r[32];
+                HS_LD32(r, tmem + lrow + kColS + 32 * ch);
+                tmem_wait_ld();
+                const uint32_t vm = sm->vmask[i & 1][ch];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                x[j] = ((vm >> j) & 1u) ? __uint_as_float(r[j]) * A.scale_log2 : -INFINITY;
-                mb = fmaxf(mb, x[j]);
+                for (int j = 0; j < 32; ++j)
+                    if ((vm >> j) & 1u) mb = fmaxf(mb, __uint_as_float(r[j]) * A.scale_log2);
             }
             const bool need = mb > m + kRescaleLog2 || (m == -INFINITY && mb > -INFINITY);
             const float m_new = need ? mb : m;
             if (i > 0 && __any_sync(0xffffffffu, need)) {
-                // O holds blocks 0..i-1 once their last product is done: rescale it to m_new
-                if (!warp_wait(sm, &sm->bar[kPvDone + ((i - 1) & 1)], ((i - 1) >> 1) & 1, A.status)) { ok = false; break; }
+                // O holds blocks 0..i-1 (their product is done: the scores of block i
+                // were computed after it): rescale it to m_new
+                if (!warp_wait(sm, &sm->bar[kPvDone], (i - 1) & 1, A.status)) { ok = false; break; }
                 fence_after();
                 const float f = need ? ex2(m - m_new) : 1.f;  // m = -inf: O is zero so far
 #pragma unroll 1
@@ -377,24 +468,30 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
                 l *= f;
             }
             m = m_new;
-            uint32_t pk[16];
+            // pass 2: P = 2^(x - m) in bf16, written over the scores already read
+#pragma unroll 1
+            for (int ch = 0; ch < kBlk / 32; ++ch) {
+                uint32_t r[32];
+                HS_LD32(r, tmem + lrow + kColS + 32 * ch);
+                tmem_wait_ld();
+                const uint32_t vm = sm->vmask[i & 1][ch];
+                uint32_t pk[16];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const float p0 = x[2 * c] == -INFINITY ? 0.f : ex2(x[2 * c] - m);
-                const float p1 = x[2 * c + 1] == -INFINITY ? 0.f : ex2(x[2 * c + 1] - m);
-                const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-                const float2 pr = __bfloat1622float2(pb);
-                l += pr.x + pr.y;
-                pk[c] = *reinterpret_cast<const uint32_t*>(&pb);
+                for (int c = 0; c < 16; ++c) {
+                    const float p0 = ((vm >> (2 * c)) & 1u) ? ex2(__uint_as_float(r[2 * c]) * A.scale_log2 - m) : 0.f;
+                    const float p1 = ((vm >> (2 * c + 1)) & 1u) ? ex2(__uint_as_float(r[2 * c + 1]) * A.scale_log2 - m) : 0.f;
+                    const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+                    const float2 pr = __bfloat1622float2(pb);
+                    l += pr.x + pr.y;
+                    pk[c] = *reinterpret_cast<const uint32_t*>(&pb);
+                }
+                HS_ST16(tmem + lrow + kColS + 16 * ch, pk);
             }
-            // P[st] was the operand of block i-2's product
-            if (i >= 2 && !warp_wait(sm, &sm->bar[kPvDone + st], ((i - 2) >> 1) & 1, A.status)) { ok = false; break; }
-            HS_ST16(tmem + lrow + kColP + 16 * st, pk);
             tmem_wait_st();
             fence_before();
-            bar_arrive(&sm->bar[kPFull + st]);
+            bar_arrive(&sm->bar[kPFull]);
         }
-        if (ok && nb > 0 && warp_wait(sm, &sm->bar[kOFull], 0, A.status)) {
+        if (ok && nb > 0 && warp_wait(sm, &sm->bar[kPvDone], (nb - 1) & 1, A.status)) {
             fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             size_t orow;
@@ -469,11 +566,14 @@ size_t attend_smem_bytes() { return kSmemBytes; }
 
 AttendPlan attend_plan(int B, int H, int k, int num_sms) {
     AttendPlan p;
-    // one CTA per SM: B requests x 2 value halves x nsplit key splits, at least 64 keys each
+    // one CTA per SM: B requests x 2 value halves x nsplit key splits, at least one
+    // 256-key block each and at most the slots one CTA stages
     int nsplit = num_sms / (2 * B);
     if (nsplit < 1) nsplit = 1;
-    const int max_split = (k + 63) / 64;
+    const int max_split = (k + kBlk - 1) / kBlk;
     if (nsplit > max_split) nsplit = max_split;
+    const int min_split = (k + kMaxSplitKeys - 1) / kMaxSplitKeys;
+    if (nsplit < min_split) nsplit = min_split;
     int per = (k + nsplit - 1) / nsplit;
     per = (per + kBlk - 1) / kBlk * kBlk;
     nsplit = (k + per - 1) / per;
