@@ -32,6 +32,8 @@ sys.path.insert(0, ROOT)
 METRIC = "top-k resolutions/s; miss-fetch GB/s vs H2D peak; µs per layer-step"
 UNIT = "resolutions/s"
 FLUSH_BYTES = 512 << 20
+ATTEND_HEADS = 128                # query heads of the attention consumer (DeepSeek-style MLA)
+ATTEND_SCALE = 576 ** -0.5         # softmax scale over the 576-dim keys
 H2D_PROBE_BYTES = 1 << 30
 
 
@@ -311,6 +313,11 @@ def run_ours(args, rank: int, world: int, dist) -> None:
         if not args.no_extras and rank == 0:
             policies = measure_policies(torch, hs, ctx, w, sel_dev, out_dev, miss_dev, flush, W, K)
 
+        # ---- the consumer: sparse attention over this step's resolved slots
+        attend = None
+        if not args.no_extras and rank == 0 and w.E == 656:
+            attend = measure_attend(torch, ctx, w, out_dev[W + K - 1], flush)
+
         # ---- decode-time append: one new entry per request per call (last, it rewrites rows)
         append = None
         if not args.no_extras and rank == 0:
@@ -386,6 +393,7 @@ def run_ours(args, rank: int, world: int, dist) -> None:
         "no_io": noio,
         "append": append,
         "policies": policies,
+        "attend": attend,
         "roofline": roofline,
         "gpu_launches": K * kpc,
         "device_status": status,
@@ -401,9 +409,10 @@ def run_ours(args, rank: int, world: int, dist) -> None:
 
 
 def run_layers(args, rank: int, world: int, dist) -> None:
-    """Quest-style pages, 8 layers sharing one selection per step: the two-stream overlap of
-    layer l+1's resolution with layer l's consumer (the checksum stand-in), against the
-    serial order and against the serial order without fetches (the miss overhead)."""
+    """8 layers sharing one selection per step: the two-stream overlap of layer l+1's
+    resolution with layer l's consumer, against the serial order and against the serial
+    order without fetches (the miss overhead). The consumer is the sparse attention
+    (hs_attend, 128 heads) for 656-byte DSA entries, else the checksum stand-in."""
     import numpy as np
     import torch
 
@@ -413,7 +422,7 @@ def run_layers(args, rank: int, world: int, dist) -> None:
 
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     __graft_entry__.build()
-    w = workload_for_rank("quest", rank)
+    w = workload_for_rank(args.workload, rank)
     K, W = args.steps, args.warmup
     T = W + K
     B, L = w.B, w.L
@@ -424,6 +433,23 @@ def run_layers(args, rank: int, world: int, dist) -> None:
     out = torch.empty((L, B, w.k), dtype=torch.int32, device="cuda")
     miss = torch.empty((T, L, B), dtype=torch.int32, device="cuda")
     sums = torch.empty((L, B), dtype=torch.int64, device="cuda")
+    attention = w.E == 656
+    if attention:
+        H = ATTEND_HEADS
+        g = torch.Generator(device="cuda").manual_seed(21)
+        qs = [torch.randn((B, H, 576), generator=g, device="cuda").to(torch.bfloat16) for _ in range(L)]
+        o_l = torch.empty((L, B, H, 512), dtype=torch.float32, device="cuda")
+        lse_l = torch.empty((L, B, H), dtype=torch.float32, device="cuda")
+        nbytes = ctxs[0].attend_workspace(B, H, w.k)
+        wss = [torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda") for _ in range(L)]
+
+    def consume(layer, stream):
+        if attention:
+            ctxs[layer].attend(qs[layer], out[layer], o_l[layer], lse_l[layer], ATTEND_SCALE,
+                               workspace=wss[layer] if nbytes else None, stream=stream)
+        else:
+            ctxs[layer].checksum_rows(out[layer], sums[layer], stream=stream)
+
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     s_res, s_use = torch.cuda.Stream(), torch.cuda.Stream()
     peak_h2d = h2d_peak_gbs(torch)
@@ -447,9 +473,9 @@ def run_layers(args, rank: int, world: int, dist) -> None:
                     ev = torch.cuda.Event()
                     ev.record(s_res)
                     s_use.wait_event(ev)
-                    ctxs[layer].checksum_rows(out[layer], sums[layer], stream=s_use)
+                    consume(layer, s_use)
                 else:
-                    ctxs[layer].checksum_rows(out[layer], sums[layer], stream=s_res)
+                    consume(layer, s_res)
             if mode == "overlap":
                 s_res.wait_stream(s_use)
             z.record(s_res)
@@ -484,7 +510,10 @@ def run_layers(args, rank: int, world: int, dist) -> None:
             "miss_bytes_per_step": miss_rows * w.E / K,
             "miss_fetch_gbs_overlapped": miss_rows * w.E / (tot["overlap"] * 1e-6) / 1e9,
             "h2d_peak_gbs": peak_h2d,
-            "consumer_bytes_per_step": B * L * w.k * w.E},
+            "consumer": (f"hs_attend: sparse MLA-style attention, {ATTEND_HEADS} heads, bf16 tensor-core "
+                         "products" if attention else "hs_checksum_rows (reads every resolved row)"),
+            "consumer_bytes_per_step": B * L * w.k * w.E,
+            "consumer_flops_per_step": (2 * B * L * ATTEND_HEADS * w.k * (576 + 512)) if attention else None},
         "device_status": status, "clocks": sampler.summary(),
     }
     if rank == 0:
@@ -536,6 +565,44 @@ def measure_policies(torch, hs, ctx, w, sel_dev, out_dev, miss_dev, flush, W: in
         curve[str(S)] = row
     return {"step": step, "misses_per_step_by_slots": curve, "trace_steps_for_curve": T,
             "seed": POLICY_SEED}
+
+
+def measure_attend(torch, ctx, w, out_slots, flush, n: int = 32) -> dict:
+    """hs_attend over one step's resolved slots: 128 heads of bf16 queries, L2 flushed
+    between calls; achieved = algorithmic FLOPs (2 H k (576 + 512) per request) / time."""
+    H = ATTEND_HEADS
+    g = torch.Generator(device="cuda").manual_seed(5)
+    q = torch.randn((w.B, H, 576), generator=g, device="cuda").to(torch.bfloat16)
+    o = torch.empty((w.B, H, 512), dtype=torch.float32, device="cuda")
+    lse = torch.empty((w.B, H), dtype=torch.float32, device="cuda")
+    nbytes = ctx.attend_workspace(w.B, H, w.k)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda") if nbytes else None
+    ctx.clear_status()
+    for _ in range(3):
+        ctx.attend(q, out_slots, o, lse, ATTEND_SCALE, workspace=ws)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record()
+        ctx.attend(q, out_slots, o, lse, ATTEND_SCALE, workspace=ws)
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    assert ctx.status() == 0
+    us = [a.elapsed_time(b) * 1e3 for a, b in evs]
+    flops = 2.0 * w.B * H * w.k * (576 + 512)
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except OSError:
+        pass
+    peak = peaks.get("bf16_tflops", 1900.0)
+    tf = flops / (statistics.mean(us) * 1e-6) / 1e12
+    return {"calls": n, "heads": H, "k": w.k, "requests": w.B, "us_per_call": statistics.mean(us),
+            "us_per_call_median": statistics.median(us), "algorithmic_flops_per_call": flops,
+            "kv_bytes_per_call": w.B * w.k * w.E,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                         "peak_source": "MEASURED_PEAKS.json bf16_tflops (of measured)" if "bf16_tflops" in peaks
+                         else "fallback 1.9 PFLOP/s"}}
 
 
 def measure_append(torch, ctx, w, flush, n: int) -> dict:
@@ -640,7 +707,7 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
-        elif args.workload == "quest":
+        elif args.workload in ("quest", "dsa_layers"):
             run_layers(args, rank, world, dist)
         else:
             run_ours(args, rank, world, dist)

@@ -70,6 +70,10 @@ WORKLOADS = {
     # 8 layers sharing one selection of 128 pages, 256 pages of buffer per layer
     "quest": Workload("quest", 5, B=64, L=8, C=4096, S=256, k=128, E=65536, kv_kind=KV_BF16,
                       T=128, keep_pct=90, zipf_s=1.1, seed=4),
+    # the DSA-style decode with 8 layers sharing one selection per step (for the
+    # layer-wise overlap of resolution and attention)
+    "dsa_layers": Workload("dsa_layers", 6, B=32, L=8, C=32768, S=4096, k=2048, E=656, kv_kind=KV_DSA656,
+                           T=64, keep_pct=90, zipf_s=1.1, recent=64, seed=5),
 }
 
 
