@@ -308,6 +308,12 @@ def run_ours(args, rank: int, world: int, dist) -> None:
             ctx.resolve_host(sel_pin[t].numpy(), out_np, miss_np)
             e2e_s += time.perf_counter() - t0
 
+        # ---- the same steps through a pooled context (requests' histories at permuted extents
+        # of one shared pinned store)
+        pooled = None
+        if not args.no_extras and rank == 0:
+            pooled = measure_pooled(torch, hs, ctx, w, sel_dev, out_dev, miss_dev, flush, W, K)
+
         # ---- replacement policies: the step under each, and misses over buffer sizes
         policies = None
         if not args.no_extras and rank == 0:
@@ -392,6 +398,7 @@ def run_ours(args, rank: int, world: int, dist) -> None:
         "kernels": kernels,
         "no_io": noio,
         "append": append,
+        "pooled": pooled,
         "policies": policies,
         "attend": attend,
         "roofline": roofline,
@@ -565,6 +572,31 @@ def measure_policies(torch, hs, ctx, w, sel_dev, out_dev, miss_dev, flush, W: in
         curve[str(S)] = row
     return {"step": step, "misses_per_step_by_slots": curve, "trace_steps_for_curve": T,
             "seed": POLICY_SEED}
+
+
+def measure_pooled(torch, hs, ctx, w, sel_dev, out_dev, miss_dev, flush, W: int, K: int) -> dict:
+    """The timed steps through hs_create_pooled over the main context's host store seen as a
+    pool of B * C rows, request b at the extent of request (7b + 3) mod B, every length C."""
+    rows = w.B * w.C
+    pc = hs.Context(w.B, w.C, w.S, w.E, pool=(ctx.host_kv_address(), rows, ctx.host_stride))
+    pc.set_extents([((7 * b + 3) % w.B) * w.C for b in range(w.B)], [w.C] * w.B)
+    stream = torch.cuda.current_stream()
+    for t in range(W):
+        pc.resolve(sel_dev[t], out_dev[t], miss_dev[t])
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        pc.resolve(sel_dev[W + i], out_dev[W + i], miss_dev[W + i])
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    us = [a.elapsed_time(b) * 1e3 for a, b in ev]
+    status = pc.status()
+    pc.close()
+    return {"us_per_layer_step": statistics.mean(us), "us_median": statistics.median(us),
+            "misses_per_step": float(miss_dev[W:].sum()) / K, "device_status": status,
+            "how": "hs_create_pooled over the same pinned store, extents permuted across requests"}
 
 
 def measure_attend(torch, ctx, w, out_slots, flush, n: int = 32) -> dict:

@@ -32,6 +32,22 @@ POLICY_LRU, POLICY_FIFO, POLICY_RANDOM = 0, 1, 2
 
 # every symbol include/hs.h declares, with (restype, argtypes)
 _VP, _I, _SZ, _U = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint
+_I64, _F64 = ctypes.c_int64, ctypes.c_double
+
+
+class PlanParams(ctypes.Structure):
+    """hs_plan_params (include/hs.h)."""
+    _fields_ = [("top_k", _I), ("device_buffer_size", _I), ("host_to_device_ratio", _F64),
+                ("entry_bytes", _I), ("layers", _I), ("context_len", _I64), ("hbm_bytes", _I64),
+                ("host_bytes", _I64), ("miss_fraction", _F64), ("link_gbs", _F64)]
+
+
+class PlanResult(ctypes.Structure):
+    """hs_plan_result (include/hs.h)."""
+    _fields_ = [("device_bytes_per_request", _I64), ("requests_by_device", _I64), ("host_pool_rows", _I64),
+                ("host_pool_bytes", _I64), ("requests_by_host", _I64), ("requests", _I64),
+                ("miss_bytes_per_step", _F64), ("link_us_per_step", _F64)]
+
 SIGNATURES = {
     "hs_create": (_VP, [_I, _I, _I, _I]),
     "hs_create_with_host": (_VP, [_I, _I, _I, _I, _VP, _SZ]),
@@ -56,6 +72,15 @@ SIGNATURES = {
     "hs_attend": (_I, [_VP, _VP, _VP, _I, _I, _VP, _I, ctypes.c_float, _VP, _VP, _VP, ctypes.c_size_t]),
     "hs_attend_workspace": (_I, [_VP, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
     "hs_kernels_per_call": (_I, [_VP]),
+    "hs_plan": (_I, [ctypes.POINTER(PlanParams), ctypes.POINTER(PlanResult)]),
+    "hs_pool_create": (_VP, [_I64]),
+    "hs_pool_destroy": (None, [_VP]),
+    "hs_pool_reserve": (_I64, [_VP, _I64]),
+    "hs_pool_release": (_I, [_VP, _I64]),
+    "hs_pool_free_rows": (_I64, [_VP]),
+    "hs_pool_largest_free": (_I64, [_VP]),
+    "hs_create_pooled": (_VP, [_I, _I, _I, _I, _VP, _I64, _SZ]),
+    "hs_set_extents": (_I, [_VP, _VP, _VP, _VP]),
     "hs_last_error": (ctypes.c_char_p, []),
     "hs_resolve_noalloc": (_I, [_VP, _I, _I, _I, _I, _VP, _SZ, _VP, _VP, _VP, _VP, _VP, _VP, _I,
                                 _VP, _VP, _VP]),
@@ -125,16 +150,66 @@ class _DeviceArray:
         self._owner = owner
 
 
+def plan(**params) -> dict:
+    """hs_plan: the concurrency and host-link time the deployment knobs admit. Keywords are
+    the fields of hs_plan_params; returns the fields of hs_plan_result as a dict."""
+    lib = load_library()
+    inp = PlanParams(**params)
+    out = PlanResult()
+    if lib.hs_plan(ctypes.byref(inp), ctypes.byref(out)) != HS_OK:
+        raise HsError(f"hs_plan refused {params}")
+    return {name: getattr(out, name) for name, _ in PlanResult._fields_}
+
+
+class Pool:
+    """Admission bookkeeping of a shared host pool of `rows` rows (hs_pool_*)."""
+
+    def __init__(self, rows: int):
+        self._lib = load_library()
+        self.rows = rows
+        self._h = self._lib.hs_pool_create(rows)
+        if not self._h:
+            raise HsError("hs_pool_create failed")
+
+    def reserve(self, n: int) -> int:
+        """Base row of a new extent of n rows, or -1 if none is long enough (first fit)."""
+        return int(self._lib.hs_pool_reserve(self._h, n))
+
+    def release(self, base: int) -> None:
+        if self._lib.hs_pool_release(self._h, base) != HS_OK:
+            raise HsError(f"no extent starts at {base}")
+
+    def free_rows(self) -> int:
+        return int(self._lib.hs_pool_free_rows(self._h))
+
+    def largest_free(self) -> int:
+        return int(self._lib.hs_pool_largest_free(self._h))
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            self._lib.hs_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+
 class Context:
     """One layer's cache for R requests (``hs_create``); release with close()."""
 
     def __init__(self, num_requests: int, context_len: int, slots: int, entry_bytes: int,
-                 share_host_with: "Context | None" = None):
+                 share_host_with: "Context | None" = None, pool=None):
         """share_host_with: borrow another context's host store (hs_create_with_host);
-        that context must outlive this one."""
+        that context must outlive this one. pool: (address, rows, stride) of a pinned host
+        pool shared through extents (hs_create_pooled); the pool must outlive this one."""
         self._lib = load_library()
         self.R, self.C, self.S, self.E = num_requests, context_len, slots, entry_bytes
-        if share_host_with is None:
+        self.pool_rows = 0
+        if pool is not None:
+            addr, rows, stride = pool
+            self.pool_rows = rows
+            self._h = self._lib.hs_create_pooled(num_requests, context_len, slots, entry_bytes, addr, rows, stride)
+        elif share_host_with is None:
             self._h = self._lib.hs_create(num_requests, context_len, slots, entry_bytes)
         else:
             self._lender = share_host_with
@@ -245,10 +320,20 @@ class Context:
 
     # ------------------------------------------------------------------ views
     def host_kv(self) -> np.ndarray:
-        """The pinned host store as a writable numpy view [R, C, host_stride] (uint8)."""
-        n = self.R * self.C * self.host_stride
-        buf = (ctypes.c_uint8 * n).from_address(self._lib.hs_host_kv(self._h))
-        return np.frombuffer(buf, dtype=np.uint8).reshape(self.R, self.C, self.host_stride)
+        """The pinned host store as a writable numpy view [R, C, host_stride] (uint8), or
+        [pool_rows, host_stride] for a pooled context."""
+        rows = self.pool_rows if self.pool_rows else self.R * self.C
+        buf = (ctypes.c_uint8 * (rows * self.host_stride)).from_address(self._lib.hs_host_kv(self._h))
+        a = np.frombuffer(buf, dtype=np.uint8)
+        return a.reshape(rows, self.host_stride) if self.pool_rows else a.reshape(self.R, self.C, self.host_stride)
+
+    def set_extents(self, base, length, stream=None) -> None:
+        """Pooled context: request b's history is rows base[b] .. base[b] + length[b] - 1 of
+        the pool; a request whose extent changes starts empty."""
+        b = np.ascontiguousarray(base, dtype=np.int64)
+        n = np.ascontiguousarray(length, dtype=np.int32)
+        self._check(self._lib.hs_set_extents(self._h, _stream(stream), b.ctypes.data, n.ctypes.data),
+                    "hs_set_extents")
 
     def host_kv_address(self) -> int:
         return int(self._lib.hs_host_kv(self._h))

@@ -14,7 +14,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libhs.so")
-SOURCES = ["hs_api.cu", "hs_kernels.cu", "hs_noalloc.cu", "hs_consume.cu", "hs_attend.cu"]
+SOURCES = ["hs_api.cu", "hs_kernels.cu", "hs_noalloc.cu", "hs_consume.cu", "hs_attend.cu", "hs_pool.cu"]
 HEADERS = [os.path.join(CSRC, "hs_internal.h"), os.path.join(ROOT, "include", "hs.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-Xptxas", "-v",

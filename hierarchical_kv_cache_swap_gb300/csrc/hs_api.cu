@@ -28,6 +28,11 @@ struct hs_ctx {
     int32_t* stage_out;    // [R][S]
     int32_t* stage_miss;   // [R]
     bool attend_ok;        // the attention kernel's shared memory fits this device
+    int64_t pool_rows;     // > 0: the host store is a shared pool of that many rows
+    int64_t* d_base;       // [R] device copies of the extents (pooled contexts)
+    int32_t* d_len;        // [R]
+    int64_t* ext_base;     // [R] host copies, to tell which requests change
+    int32_t* ext_len;      // [R]
 };
 
 namespace {
@@ -59,6 +64,10 @@ void free_ctx(hs_ctx* h) {
     cudaFree(h->stage_sel);
     cudaFree(h->stage_out);
     cudaFree(h->stage_miss);
+    cudaFree(h->d_base);
+    cudaFree(h->d_len);
+    free(h->ext_base);
+    free(h->ext_len);
     free(h);
 }
 
@@ -104,9 +113,10 @@ const char* hs_last_error(void) { return g_err; }
 
 namespace {
 
-// Shared by hs_create (host_kv == nullptr: allocate the store) and hs_create_with_host.
+// Shared by hs_create (host_kv == nullptr: allocate the store), hs_create_with_host and
+// hs_create_pooled (pool_rows > 0: the store is a shared pool addressed through extents).
 hs_ctx* create(int num_requests, int context_len, int slots, int entry_bytes, uint8_t* host_kv,
-               size_t host_stride) {
+               size_t host_stride, int64_t pool_rows = 0) {
     const int R = num_requests, C = context_len, S = slots, E = entry_bytes;
     if (R <= 0 || C <= 0 || S <= 0 || E <= 0) {
         fail(HS_ERR_INVALID, "all sizes must be positive (R=%d C=%d S=%d E=%d)", R, C, S, E);
@@ -201,6 +211,26 @@ hs_ctx* create(int num_requests, int context_len, int slots, int entry_bytes, ui
     HS_ALLOC(h->stage_sel, sizeof(int32_t) * (size_t)R * S);
     HS_ALLOC(h->stage_out, sizeof(int32_t) * (size_t)R * S);
     HS_ALLOC(h->stage_miss, sizeof(int32_t) * (size_t)R);
+    if (pool_rows > 0) {
+        h->pool_rows = pool_rows;
+        HS_ALLOC(h->d_base, sizeof(int64_t) * (size_t)R);
+        HS_ALLOC(h->d_len, sizeof(int32_t) * (size_t)R);
+        h->ext_base = (int64_t*)calloc((size_t)R, sizeof(int64_t));
+        h->ext_len = (int32_t*)calloc((size_t)R, sizeof(int32_t));
+        if (!h->ext_base || !h->ext_len) {
+            fail(HS_ERR_NOMEM, "out of host memory");
+            free_ctx(h);
+            return nullptr;
+        }
+        if ((e = cudaMemset(h->d_base, 0, sizeof(int64_t) * (size_t)R)) != cudaSuccess ||
+            (e = cudaMemset(h->d_len, 0, sizeof(int32_t) * (size_t)R)) != cudaSuccess) {
+            cuda_fail(e, "cudaMemset");
+            free_ctx(h);
+            return nullptr;
+        }
+        L.row_base = h->d_base;
+        L.row_len = h->d_len;
+    }
 #undef HS_ALLOC
 
     if ((e = hs::configure_kernels(dev)) != cudaSuccess) {
@@ -243,6 +273,49 @@ hs_ctx* hs_create_with_host(int num_requests, int context_len, int slots, int en
         return nullptr;
     }
     return create(num_requests, context_len, slots, entry_bytes, host_kv, host_stride);
+}
+
+hs_ctx* hs_create_pooled(int num_requests, int context_len, int slots, int entry_bytes, const void* host_pool,
+                         int64_t pool_rows, size_t host_stride) {
+    if (!host_pool || ((uintptr_t)host_pool & 15) || host_stride % 16 != 0 || host_stride < (size_t)entry_bytes ||
+        entry_bytes <= 0 || pool_rows <= 0) {
+        fail(HS_ERR_INVALID, "host_pool must be 16-byte aligned, pool_rows > 0 and host_stride a multiple of 16 "
+                             ">= entry_bytes");
+        return nullptr;
+    }
+    return create(num_requests, context_len, slots, entry_bytes, (uint8_t*)host_pool, host_stride, pool_rows);
+}
+
+int hs_set_extents(hs_ctx* h, hs_stream_t stream, const int64_t* base, const int32_t* len) {
+    if (!h) return fail(HS_ERR_INVALID, "null context");
+    if (h->pool_rows <= 0) return fail(HS_ERR_INVALID, "the context was not created on a pool");
+    if (!base || !len) return fail(HS_ERR_INVALID, "null base/len");
+    const hs::Layout& L = h->L;
+    for (int b = 0; b < L.R; ++b)
+        if (base[b] < 0 || len[b] < 0 || len[b] > L.C || base[b] + len[b] > h->pool_rows)
+            return fail(HS_ERR_INVALID, "request %d: extent [%lld, +%d) outside [0, %lld) or len > %d", b,
+                        (long long)base[b], len[b], (long long)h->pool_rows, L.C);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e;
+    for (int b = 0; b < L.R; ++b) {
+        if (base[b] == h->ext_base[b] && len[b] == h->ext_len[b]) continue;
+        // a new request in row b: its cache state starts empty
+        if ((e = cudaMemsetAsync(L.pt + (size_t)b * L.C, 0xff, sizeof(int32_t) * (size_t)L.C, s)) != cudaSuccess ||
+            (e = cudaMemsetAsync(L.tok + (size_t)b * L.S, 0xff, sizeof(int32_t) * (size_t)L.S, s)) != cudaSuccess ||
+            (e = cudaMemsetAsync(L.lu + (size_t)b * L.S, 0xff, sizeof(int32_t) * (size_t)L.S, s)) != cudaSuccess ||
+            (e = cudaMemsetAsync(L.step + b, 0, sizeof(int32_t), s)) != cudaSuccess ||
+            (e = cudaMemsetAsync(L.dev + (size_t)b * L.S * L.E, 0, (size_t)L.S * L.E, s)) != cudaSuccess)
+            return cuda_fail(e, "cudaMemsetAsync");
+        h->ext_base[b] = base[b];
+        h->ext_len[b] = len[b];
+    }
+    if ((e = cudaMemcpyAsync(h->d_base, h->ext_base, sizeof(int64_t) * (size_t)L.R, cudaMemcpyHostToDevice, s)) !=
+            cudaSuccess ||
+        (e = cudaMemcpyAsync(h->d_len, h->ext_len, sizeof(int32_t) * (size_t)L.R, cudaMemcpyHostToDevice, s)) !=
+            cudaSuccess)
+        return cuda_fail(e, "cudaMemcpyAsync");
+    g_err[0] = 0;
+    return HS_OK;
 }
 
 int hs_append(hs_ctx* h, hs_stream_t stream, const uint8_t* kv, const int32_t* positions, int B) {

@@ -56,15 +56,15 @@ checksum_kernel(const uint8_t* __restrict__ dev, int S, int E, const int32_t* __
 constexpr int kAppendThreads = 256;
 
 // Decode-time append: row kv[b] joins request b's history at position pos[b] in the
-// host store (zero-copy stores over the host link) and, when that position is
-// resident, its device slot. Grid (parts, R); CTA (part, b) copies its share of the
+// host store (zero-copy stores over the host link; in a pooled store, row base[b] + p)
+// and, when that position is resident, its device slot. Grid (parts, R); CTA (part, b) copies its share of the
 // row's 16-byte chunks.
 __global__ void __launch_bounds__(kAppendThreads)
 append_kernel(const Layout L, const uint8_t* __restrict__ kv, const int32_t* __restrict__ pos) {
     const int b = blockIdx.y;
     const int32_t p = __ldg(pos + b);
     if (p < 0) return;  // no new entry for this request
-    if (p >= L.C) {
+    if (p >= (L.row_len ? __ldg(L.row_len + b) : L.C)) {
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(L.status, 1u /* HS_STATUS_RANGE */);
         return;
     }
@@ -73,7 +73,8 @@ append_kernel(const Layout L, const uint8_t* __restrict__ kv, const int32_t* __r
     const uint32_t per = (cpr + gridDim.x - 1) / gridDim.x;
     const uint32_t c0 = blockIdx.x * per, c1 = min(c0 + per, cpr);
     const uint4* src = reinterpret_cast<const uint4*>(kv + (size_t)b * L.E);
-    uint4* host = reinterpret_cast<uint4*>(const_cast<uint8_t*>(L.host) + ((size_t)b * L.C + p) * L.host_stride);
+    const int64_t row = (L.row_base ? __ldg(L.row_base + b) : (int64_t)b * L.C) + p;
+    uint4* host = reinterpret_cast<uint4*>(const_cast<uint8_t*>(L.host) + (size_t)row * L.host_stride);
     uint4* dev = s >= 0 ? reinterpret_cast<uint4*>(L.dev + ((size_t)b * L.S + s) * L.E) : nullptr;
     for (uint32_t c = c0 + threadIdx.x; c < c1; c += kAppendThreads) {
         const uint4 v = __ldg(src + c);

@@ -46,6 +46,8 @@ struct Layout {
     uint32_t* ready_pos;   // [R]: (tag mod 2^16) << 16 | list length, once request b's list is published
     uint32_t* ready_slot;  // [R]: == tag once request b's answers (out_slots) are written
     uint32_t* gcount;      // [R + G]: fetch CTA counters; (b, share q) at b + q*R; tag = gcount[b] + 1
+    const int64_t* row_base = nullptr;  // [R] pooled store: first row of request b (else b * C)
+    const int32_t* row_len = nullptr;   // [R] pooled store: positions request b has (else C)
     int policy = kPolicyLru;  // replacement policy of the calls launched with this layout
     uint64_t seed = 0;        // kPolicyRandom's seed
 };

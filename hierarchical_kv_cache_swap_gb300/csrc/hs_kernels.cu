@@ -210,13 +210,15 @@ struct Request {
     uint32_t* scratch;
     uint16_t* sa;
     uint16_t* sb;
+    int lim;  // positions this request has: C, or its extent's length in a pooled store
     uint32_t m = 0, N = 0, miss_base = 0, cand_base = 0;
     int g0 = 0, g1 = 0, s0 = 0, s1 = 0;  // this thread's miss-bitmap groups and slot range
     const uint16_t* victims = nullptr;  // victims[r] = slot of the r-th miss
 
     __device__ Request(const Layout& L_, const Plan& P_, uint8_t* smem_, const int32_t* sel, int k_,
                        int32_t* out)
-        : L(L_), P(P_), smem(smem_), b(blockIdx.x), k(k_) {
+        : L(L_), P(P_), smem(smem_), b(blockIdx.x), k(k_),
+          lim(L_.row_len ? __ldg(L_.row_len + blockIdx.x) : L_.C) {
         selb = sel + (size_t)b * k;
         outb = out + (size_t)b * k;
         ptb = L.pt + (size_t)b * L.C;
@@ -262,7 +264,7 @@ struct Request {
                                                const int32_t* extra = nullptr,
                                                int32_t* extra_out = nullptr) const {
         const int tid = threadIdx.x;
-        const int C = L.C;
+        const int C = lim;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int j = j0 + q * NT + tid;
@@ -287,7 +289,7 @@ struct Request {
     // Returns true (block-uniform) if any selection missed.
     __device__ bool probe(int32_t (&p)[4], int32_t (&s)[4]) {
         const int tid = threadIdx.x;
-        const int C = L.C;
+        const int C = lim;
         uint32_t st = 0;
         int any_miss = 0;
         for (int j0 = 0; j0 < k; j0 += 4 * NT) {
@@ -478,7 +480,7 @@ struct Request {
 
     // 4c. answers for the missed selections (their rank through the bitmap).
     __device__ __forceinline__ void answer(int j, int32_t p) {
-        if (p < 0 || p >= L.C) return;
+        if (p < 0 || p >= lim) return;
         const int w = p >> 5;
         const uint32_t bit = 1u << (p & 31);
         const uint32_t word = posbm[w];
@@ -580,7 +582,7 @@ __device__ __forceinline__ void fetch_rows(const Layout& L, const int32_t* out, 
     const int32_t* gpos = L.fpos + (size_t)b * L.S;
     const int32_t* gsel = L.fsel + (size_t)b * L.S;
     const int32_t* ob = out + (size_t)b * k;
-    const uint8_t* hb = L.host + (size_t)b * L.C * L.host_stride;
+    const uint8_t* hb = L.host + (size_t)(L.row_base ? __ldg(L.row_base + b) : (int64_t)b * L.C) * L.host_stride;
     uint8_t* db = L.dev + (size_t)b * L.S * L.E;
     bool slots_known = false;
     for (uint32_t base = 0; base < n; base += GT * kGatherUnroll) {

@@ -256,6 +256,80 @@ int hs_set_flags(hs_ctx* ctx, unsigned flags);
  */
 int hs_set_policy(hs_ctx* ctx, int policy, uint64_t seed);
 
+/*
+ * ---------------------------------------------------------------------------------
+ * Capacity planning and the shared host pool (blog commentary, section on deployment
+ * knobs: top_k, device_buffer_size and host_to_device_ratio set HiSparse's working range;
+ * 2048 / 6144 / 10 for a disaggregated decode instance, a 4096 buffer with ratio 8 for a
+ * colocated 8-GPU node). Host code only; nothing here touches a GPU.
+ */
+typedef struct {
+    int top_k;                   /* selections per request, layer and step (k) */
+    int device_buffer_size;      /* device slots per request and layer (S), >= top_k */
+    double host_to_device_ratio; /* host pool rows / device pool rows, > 0 */
+    int entry_bytes;             /* bytes of one KV entry (E) */
+    int layers;                  /* layers, each with its own buffer and history */
+    int64_t context_len;         /* positions of history a request reserves (C) */
+    int64_t hbm_bytes;           /* device memory available to the caches */
+    int64_t host_bytes;          /* pinned host memory available to the pool */
+    double miss_fraction;        /* expected misses per step as a fraction of top_k, in [0, 1] */
+    double link_gbs;             /* host-to-device bandwidth for the fetches (0: no estimate) */
+} hs_plan_params;
+
+typedef struct {
+    int64_t device_bytes_per_request; /* all layers: buffer, page table, slot tables, miss lists */
+    int64_t requests_by_device;       /* requests whose device state fits hbm_bytes */
+    int64_t host_pool_rows;           /* ratio x requests_by_device x S, clamped to host_bytes */
+    int64_t host_pool_bytes;          /* host_pool_rows x entry_bytes x layers */
+    int64_t requests_by_host;         /* requests whose context_len rows fit the pool */
+    int64_t requests;                 /* admissible concurrency: the smaller of the two */
+    double miss_bytes_per_step;       /* host-to-device bytes of one decode step at that concurrency */
+    double link_us_per_step;          /* that traffic at link_gbs (0 when link_gbs is 0) */
+} hs_plan_result;
+
+/* hs_plan -- fills *out from *in. Returns HS_OK or HS_ERR_INVALID (a value out of range). */
+int hs_plan(const hs_plan_params* in, hs_plan_result* out);
+
+/*
+ * hs_pool -- the admission side of a shared host pool of `rows` rows: a request is
+ * admitted by reserving a contiguous extent for its whole history (first fit: the free
+ * extent with the lowest base that is long enough), and its extent is released when it
+ * finishes (merged with free neighbours). The pool only does the bookkeeping; the rows
+ * themselves are a pinned, mapped store the caller allocates (see hs_create_pooled).
+ *   hs_pool_create   NULL if rows <= 0 or out of memory; hs_pool_destroy frees it.
+ *   hs_pool_reserve  base row of a new extent of n > 0 rows, or -1 if none is long enough.
+ *   hs_pool_release  frees the extent reserved at `base`: HS_OK, or HS_ERR_INVALID if no
+ *                    extent starts there.
+ *   hs_pool_free_rows, hs_pool_largest_free   free rows in total, and in one extent.
+ */
+typedef struct hs_pool hs_pool;
+hs_pool* hs_pool_create(int64_t rows);
+void hs_pool_destroy(hs_pool* pool);
+int64_t hs_pool_reserve(hs_pool* pool, int64_t n);
+int hs_pool_release(hs_pool* pool, int64_t base);
+int64_t hs_pool_free_rows(const hs_pool* pool);
+int64_t hs_pool_largest_free(const hs_pool* pool);
+
+/*
+ * hs_create_pooled -- hs_create over a shared host pool: the caller's pinned, mapped
+ * store of pool_rows rows host_stride bytes apart (16-byte aligned, stride a multiple of
+ * 16 >= entry_bytes; the caller keeps it alive until hs_destroy). Request b reads its
+ * position p from row base[b] + p, and only positions p < len[b] exist (others are out of
+ * range: slot -1, HS_STATUS_RANGE); context_len is the longest len allowed. Initially
+ * every len is 0 (nothing admitted). Returns NULL on failure, as hs_create.
+ */
+hs_ctx* hs_create_pooled(int num_requests, int context_len, int slots, int entry_bytes, const void* host_pool,
+                         int64_t pool_rows, size_t host_stride);
+
+/*
+ * hs_set_extents -- the extents of all num_requests requests of a pooled context (host
+ * arrays base[R] >= 0, len[R] in [0, context_len], base + len <= pool_rows). Every request
+ * whose extent changes is a new request: its cache state (page table, slots, stamps,
+ * call counter, slot contents) is emptied. Enqueued on `stream` (copies from the caller's
+ * arrays, which may be reused on return). Returns HS_OK, HS_ERR_INVALID or HS_ERR_CUDA.
+ */
+int hs_set_extents(hs_ctx* ctx, hs_stream_t stream, const int64_t* base, const int32_t* len);
+
 /* Number of kernels one hs_resolve call enqueues under the current flags. */
 int hs_kernels_per_call(hs_ctx* ctx);
 

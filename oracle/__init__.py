@@ -75,6 +75,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.orc_splitmix64.restype = u64
         lib.orc_random_key.argtypes = [u64, i32, i32, i32]
         lib.orc_random_key.restype = ctypes.c_uint32
+        lib.orc_set_len.argtypes = [vp, i32, i32]
+        lib.orc_set_len.restype = i32
+        lib.orc_reset_request.argtypes = [vp, i32]
+        lib.orc_reset_request.restype = i32
         f64 = ctypes.c_double
         lib.orc_e4m3.argtypes = [ctypes.c_uint8]
         lib.orc_e4m3.restype = f64
@@ -125,6 +129,16 @@ class Oracle:
         for b, i in enumerate(ids):
             if self._lib.orc_set_request_id(self._h, b, int(i)) != 0:
                 raise ValueError("orc_set_request_id refused")
+
+    def set_len(self, b: int, n: int) -> None:
+        """Request b has positions [0, n) only (a shared pool's extent length)."""
+        if self._lib.orc_set_len(self._h, b, n) != 0:
+            raise ValueError("orc_set_len refused")
+
+    def reset_request(self, b: int) -> None:
+        """A new request takes over row b: its state starts empty."""
+        if self._lib.orc_reset_request(self._h, b) != 0:
+            raise ValueError("orc_reset_request refused")
 
     def close(self) -> None:
         if self._h:
@@ -212,6 +226,16 @@ class Oracle:
         if rc < 0:
             raise ValueError(f"orc_attend failed ({rc})")
         return out, lse, absw
+
+    def append_request(self, b: int, host_b, host_stride: int, p: int, row: np.ndarray) -> int:
+        """Decode-time append for request b alone: host_b is its history's row 0 (address or
+        array); returns the status word."""
+        row = np.ascontiguousarray(row, dtype=np.uint8)
+        haddr = host_b if isinstance(host_b, int) else host_b.ctypes.data
+        rc = self._lib.orc_append(self._h, b, haddr, host_stride, int(p), row.ctypes.data)
+        if rc < 0:
+            raise ValueError(f"orc_append failed ({rc})")
+        return rc
 
     def append(self, host: np.ndarray, positions, rows: np.ndarray) -> int:
         """Decode-time append for all R requests: host [R][C][stride] (written), positions

@@ -77,6 +77,7 @@ typedef struct {
     int32_t* t;   /* [R]       calls made so far for the request      */
     uint8_t* dev; /* [R][S][E] contents of the device slots           */
     int32_t* rid; /* [R]       request number of each row (RANDOM keys) */
+    int32_t* len; /* [R]       positions each request has (C unless set: a shared pool) */
     int policy;   /* ORC_POLICY_*, LRU unless set                     */
     uint64_t seed;/* the RANDOM policy's seed                         */
 } orc_state;
@@ -92,11 +93,12 @@ orc_state* orc_create(int R, int C, int S, int E) {
     o->t = (int32_t*)calloc((size_t)R, sizeof(int32_t));
     o->dev = (uint8_t*)calloc((size_t)R * S, (size_t)E);
     o->rid = (int32_t*)malloc(sizeof(int32_t) * (size_t)R);
-    if (!o->pt || !o->tok || !o->lu || !o->t || !o->dev || !o->rid) {
-        free(o->pt); free(o->tok); free(o->lu); free(o->t); free(o->dev); free(o->rid); free(o);
+    o->len = (int32_t*)malloc(sizeof(int32_t) * (size_t)R);
+    if (!o->pt || !o->tok || !o->lu || !o->t || !o->dev || !o->rid || !o->len) {
+        free(o->pt); free(o->tok); free(o->lu); free(o->t); free(o->dev); free(o->rid); free(o->len); free(o);
         return NULL;
     }
-    for (int b = 0; b < R; ++b) o->rid[b] = b;
+    for (int b = 0; b < R; ++b) { o->rid[b] = b; o->len[b] = C; }
     for (size_t i = 0; i < (size_t)R * C; ++i) o->pt[i] = -1;
     for (size_t i = 0; i < (size_t)R * S; ++i) { o->tok[i] = -1; o->lu[i] = -1; }
     return o;
@@ -104,7 +106,29 @@ orc_state* orc_create(int R, int C, int S, int E) {
 
 void orc_destroy(orc_state* o) {
     if (!o) return;
-    free(o->pt); free(o->tok); free(o->lu); free(o->t); free(o->dev); free(o->rid); free(o);
+    free(o->pt); free(o->tok); free(o->lu); free(o->t); free(o->dev); free(o->rid); free(o->len); free(o);
+}
+
+/*
+ * A shared host pool holds requests of different lengths: request b has positions
+ * [0, len) only (its history sits at its own extent of the pool; the caller passes that
+ * extent as host_b), and a position >= len is out of range like one >= C. A request that
+ * takes over row b is new: orc_reset_request empties its state (tables, stamps, call
+ * counter, slot contents).
+ */
+int orc_set_len(orc_state* o, int b, int32_t len) {
+    if (!o || b < 0 || b >= o->R || len < 0 || len > o->C) return ORC_EINVAL;
+    o->len[b] = len;
+    return 0;
+}
+
+int orc_reset_request(orc_state* o, int b) {
+    if (!o || b < 0 || b >= o->R) return ORC_EINVAL;
+    for (int p = 0; p < o->C; ++p) o->pt[(size_t)b * o->C + p] = -1;
+    for (int s = 0; s < o->S; ++s) { o->tok[(size_t)b * o->S + s] = -1; o->lu[(size_t)b * o->S + s] = -1; }
+    o->t[b] = 0;
+    memset(o->dev + (size_t)b * o->S * o->E, 0, (size_t)o->S * o->E);
+    return 0;
 }
 
 /* Replacement policy for the calls that follow (the state kept so far carries over). */
@@ -169,6 +193,7 @@ int orc_resolve_request(orc_state* o, int b, const uint8_t* host_b, size_t host_
     if (!o || b < 0 || b >= o->R || k <= 0 || k > o->S || !host_b || !sel_b || !out_b || !miss_b)
         return ORC_EINVAL;
     const int C = o->C, S = o->S, E = o->E;
+    const int32_t lim = o->len[b];  /* positions this request has */
     int32_t* pt = o->pt + (size_t)b * C;
     int32_t* tok = o->tok + (size_t)b * S;
     int32_t* lu = o->lu + (size_t)b * S;
@@ -187,7 +212,7 @@ int orc_resolve_request(orc_state* o, int b, const uint8_t* host_b, size_t host_
         int32_t p = sel_b[j];
         out_b[j] = -1;
         if (p < 0) continue;                         /* padding */
-        if (p >= C) { status |= ORC_ERR_RANGE; continue; }
+        if (p >= lim) { status |= ORC_ERR_RANGE; continue; }
         if (pt[p] >= 0) {
             out_b[j] = pt[p];
             hit[pt[p]] = 1;
@@ -208,7 +233,7 @@ int orc_resolve_request(orc_state* o, int b, const uint8_t* host_b, size_t host_
         int32_t* Q = (int32_t*)malloc(sizeof(int32_t) * (size_t)k);
         if (!Q) { free(hit); free(P); free(V); return ORC_ENOMEM; }
         int nq = 0;
-        for (int j = 0; j < k; ++j) if (sel_b[j] >= 0 && sel_b[j] < C) Q[nq++] = sel_b[j];
+        for (int j = 0; j < k; ++j) if (sel_b[j] >= 0 && sel_b[j] < lim) Q[nq++] = sel_b[j];
         qsort(Q, (size_t)nq, sizeof(int32_t), cmp_int);
         for (int i = 1; i < nq; ++i) if (Q[i] == Q[i - 1]) status |= ORC_ERR_DUP;
         free(Q);
@@ -235,7 +260,7 @@ int orc_resolve_request(orc_state* o, int b, const uint8_t* host_b, size_t host_
     }
     for (int j = 0; j < k; ++j) {
         int32_t p = sel_b[j];
-        if (p >= 0 && p < C && out_b[j] < 0) out_b[j] = pt[p];
+        if (p >= 0 && p < lim && out_b[j] < 0) out_b[j] = pt[p];
     }
 
     /* 5. stamps and counters (FIFO keeps the fill call of a hit slot) */
@@ -281,7 +306,7 @@ int orc_resolve(orc_state* o, const uint8_t* host, size_t host_stride, const int
 int orc_append(orc_state* o, int b, uint8_t* host_b, size_t host_stride, int32_t p, const uint8_t* row) {
     if (!o || b < 0 || b >= o->R || !host_b || !row) return ORC_EINVAL;
     if (p < 0) return 0;
-    if (p >= o->C) return ORC_ERR_RANGE;
+    if (p >= o->len[b]) return ORC_ERR_RANGE;
     memcpy(host_b + (size_t)p * host_stride, row, (size_t)o->E);
     const int32_t s = o->pt[(size_t)b * o->C + p];
     if (s >= 0) memcpy(o->dev + ((size_t)b * o->S + s) * o->E, row, (size_t)o->E);

@@ -10,6 +10,7 @@ import pytest
 
 from tests import test_oracle_attend as attend_pins
 from tests import test_oracle_pins as pins
+from tests import test_pool_plan as pool_pins
 
 MUTANTS = {
     "tie_break_reversed": ("return (x->slot > y->slot) - (x->slot < y->slot);",
@@ -33,6 +34,9 @@ MUTANTS = {
     "attend_padding_clamped": ("const int32_t sl = out_b[j];", "const int32_t sl = out_b[j] < 0 ? 0 : out_b[j];"),
     "e4m3_bias_8": ("else v = ldexp(1.0 + (double)m / 8.0, e - 7);", "else v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
     "e4m3_subnormal_scale": ("if (e == 0) v = ldexp((double)m / 8.0, -6);", "if (e == 0) v = ldexp((double)m / 8.0, -7);"),
+    "length_ignored_in_range": ("if (p >= lim) { status |= ORC_ERR_RANGE; continue; }",
+                                "if (p >= C) { status |= ORC_ERR_RANGE; continue; }"),
+    "reset_keeps_call_counter": ("    o->t[b] = 0;\n    memset(", "    memset("),
     "fifo_restamps_hits": ("if (o->policy != ORC_POLICY_FIFO)\n", "if (1)\n"),
     "random_key_low_bits": ("+ (uint64_t)s) >> 32);", "+ (uint64_t)s));"),
     "random_key_ignores_request": ("orc_random_key(o->seed, o->rid[b], t, s)", "orc_random_key(o->seed, b, t, s)"),
@@ -42,6 +46,7 @@ MUTANTS = {
 
 
 def _pin_suite(Oracle, path):
+    pool_pins.run_length_limit(Oracle, path)
     attend_pins.run_attend(Oracle, path)
     pins.run_policies(Oracle, path)
     pins.run_append(Oracle, path)
