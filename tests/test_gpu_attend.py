@@ -236,6 +236,34 @@ def test_attend_full_size_dsa_sampled():
     ctx.close()
 
 
+def test_attend_in_a_cuda_graph_equals_eager():
+    """hs_attend is enqueue-only: captured in a graph and replayed, it gives the eager result."""
+    w = tracegen.Workload("attg", 13, B=4, L=1, C=2048, S=512, k=384, E=656, kv_kind=tracegen.KV_DSA656,
+                          T=3, keep_pct=70, zipf_s=1.1, seed=5)
+    ctx, sel, out = resolved_context(w, w.T, w.B)
+    H = 128
+    q = bf16_tensor(np.random.default_rng(2).standard_normal((w.B, H, 576))).cuda()
+    nbytes = ctx.attend_workspace(w.B, H, w.k)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda") if nbytes else None
+    o_e = torch.empty((w.B, H, 512), device="cuda")
+    l_e = torch.empty((w.B, H), device="cuda")
+    ctx.attend(q, out, o_e, l_e, 0.05, workspace=ws)
+    o_g = torch.zeros_like(o_e)
+    l_g = torch.zeros_like(l_e)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            ctx.attend(q, out, o_g, l_g, 0.05, workspace=ws, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o_e, o_g) and torch.equal(l_e, l_g)
+    assert ctx.status() == 0
+    ctx.close()
+
+
 def test_attend_rejects_bad_calls():
     ctx = hs.Context(2, 64, 32, 656)
     q = torch.zeros((2, 8, 576), dtype=torch.bfloat16, device="cuda")

@@ -122,3 +122,40 @@ def test_pooled_context_rejects_bad_extents():
     with pytest.raises(hs.HsError):
         plain.set_extents([0], [1])
     plain.close()
+
+
+def test_pooled_resolution_in_a_cuda_graph():
+    """A pooled context's resolutions captured in a graph and replayed equal the eager ones
+    of a second pooled context over the same pool and extents."""
+    rng = np.random.default_rng(4)
+    R, Cmax, S, E, k, T = 3, 800, 128, 656, 64, 8
+    rows = 4000
+    pool_mem = torch.empty(rows * E, dtype=torch.uint8).pin_memory()
+    pool_mem.numpy()[:] = rng.integers(0, 256, size=rows * E, dtype=np.uint8)
+    lens = [700, 300, 800]
+    bases = [2500, 40, 1200]
+    sel = torch.from_numpy(_trace(rng, R, lens, Cmax, k, T)).cuda()
+    outs = []
+    for graph in (False, True):
+        ctx = hs.Context(R, Cmax, S, E, pool=(pool_mem.data_ptr(), rows, E))
+        ctx.set_extents(bases, lens)
+        out = torch.full((T, R, k), -9, dtype=torch.int32, device="cuda")
+        miss = torch.empty((T, R), dtype=torch.int32, device="cuda")
+        if graph:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    for t in range(T):
+                        ctx.resolve(sel[t], out[t], miss[t], stream=s)
+            torch.cuda.current_stream().wait_stream(s)
+            g.replay()
+        else:
+            for t in range(T):
+                ctx.resolve(sel[t], out[t], miss[t])
+        torch.cuda.synchronize()
+        outs.append((out.clone(), miss.clone(), ctx.page_table().clone(), ctx.device_kv().clone()))
+        ctx.close()
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
