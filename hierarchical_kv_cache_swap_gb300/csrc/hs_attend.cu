@@ -57,8 +57,8 @@ constexpr int kVKeys = 64;                           // keys per V chunk
 constexpr int kVFills = kBlk / kVKeys;               // V chunks per block
 constexpr int kFills = kKFills + kVFills;            // stage fills per block
 constexpr uint32_t kVSub = kVKeys * 128;             // bytes of one 64-dimension column of a V chunk
-constexpr int kSoftWarps = 4, kProdWarps = 16;
-constexpr int kThreads = (kSoftWarps + kProdWarps + 1) * 32;  // 672
+constexpr int kSoftWarps = 8, kProdWarps = 16;  // softmax: two groups of 4 warps, 128 keys each
+constexpr int kThreads = (kSoftWarps + kProdWarps + 1) * 32;  // 800
 constexpr int kMmaWarp = kSoftWarps + kProdWarps;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256;  // O: 256 columns; S: 256 columns, P (bf16) written over its first 128
@@ -67,12 +67,15 @@ constexpr uint32_t kWaitLimit = 1u << 22;  // polls of an mbarrier before giving
 constexpr int kMaxSplitKeys = 2048;        // slots of one split staged in shared memory
 
 // barrier indices
-enum { kQFull = 0, kFull = 1, kFree = 3, kSFull = 5, kPFull = 6, kPvDone = 7, kVmFull = 8, kDrain = 10, kBars = 11 };
+enum { kQFull = 0, kFull = 1, kFree = 3, kSFull = 5, kPFull = 6, kPvDone = 7, kVmFull = 8, kDrain = 10,
+       kBmax = 11 /* 2, by block parity */, kLsum = 13, kBars = 14 };
 
 struct Smem {  // beyond Q and the stages
     int32_t slot[kMaxSplitKeys];  // this split's out_slots
     uint64_t bar[kBars];
     uint32_t vmask[2][kBlk / 32];  // valid keys of a block, by block parity
+    float bmax[2][2][kHeads];      // [block parity][softmax group][head]: the groups' block maxima
+    float lsum[2][kHeads];         // [softmax group][head]: the groups' running sums, at the end
     uint32_t tmem;
     volatile int abort;
 };
@@ -237,6 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
         bar_init(&sm->bar[kPFull], kSoftWarps * 32);
         bar_init(&sm->bar[kPvDone], 1);
         bar_init(&sm->bar[kDrain], 1);
+        bar_init(&sm->bar[kBmax], kSoftWarps * 32);
+        bar_init(&sm->bar[kBmax + 1], kSoftWarps * 32);
+        bar_init(&sm->bar[kLsum], kSoftWarps * 32);
         sm->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -412,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
                     const uint32_t vb = k0 + st * kStageBytes;
 #pragma unroll
                     for (int ks = 0; ks < kVKeys / 16; ++ks)
-                        mma_ts(tmem + kColO, tmem + kColS + (kVKeys / 2) * vc + 8 * ks,
+                        mma_ts(tmem + kColO, tmem + kColS + (kVKeys / 2) * vc + 8 * ks + (vc >= kVFills / 2 ? 64 : 0),
                                smem_desc(vb + ks * 2048, kVSub, 1024), id_o, (i > 0 || vc > 0 || ks > 0) ? 1u : 0u);
                     mma_commit(&sm->bar[kFree + st]);
                 }
@@ -426,19 +432,25 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax (thread = head row)
-        const int h = tid;
-        const uint32_t lrow = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lanes
+        // ------------------------------------------------------------ softmax
+        // Two groups of 4 warps; thread = head row (its TMEM lane) in both. Group g reads the
+        // scores of keys [128 g, 128 g + 128) and writes their P over its own first 64
+        // columns of them (keys 0..127 -> columns 0..63, keys 128..255 -> 128..191), so
+        // neither group overwrites scores the other has yet to read. The groups share the
+        // block maximum through shared memory and keep partial running sums.
+        const int grp = warp >> 2;
+        const int h = tid & (kHeads - 1);
+        const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lanes
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int i = 0; i < nb; ++i) {
             if (!warp_wait(sm, &sm->bar[kSFull], i & 1, A.status) ||
                 !warp_wait(sm, &sm->bar[kVmFull + (i & 1)], (i >> 1) & 1, A.status)) { ok = false; break; }
             fence_after();
-            // pass 1: the block's maximum
+            // pass 1: this group's part of the block maximum, then the block's
             float mb = -INFINITY;
 #pragma unroll 1
-            for (int ch = 0; ch < kBlk / 32; ++ch) {
+            for (int ch = 4 * grp; ch < 4 * grp + 4; ++ch) {
                 uint32_t r[32];
                 HS_LD32(r, tmem + lrow + kColS + 32 * ch);
                 tmem_wait_ld();
@@ -447,16 +459,20 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
                 for (int j = 0; j < 32; ++j)
                     if ((vm >> j) & 1u) mb = fmaxf(mb, __uint_as_float(r[j]) * A.scale_log2);
             }
+            sm->bmax[i & 1][grp][h] = mb;
+            bar_arrive(&sm->bar[kBmax + (i & 1)]);
+            if (!warp_wait(sm, &sm->bar[kBmax + (i & 1)], (i >> 1) & 1, A.status)) { ok = false; break; }
+            mb = fmaxf(sm->bmax[i & 1][0][h], sm->bmax[i & 1][1][h]);
             const bool need = mb > m + kRescaleLog2 || (m == -INFINITY && mb > -INFINITY);
             const float m_new = need ? mb : m;
             if (i > 0 && __any_sync(0xffffffffu, need)) {
                 // O holds blocks 0..i-1 (their product is done: the scores of block i
-                // were computed after it): rescale it to m_new
+                // were computed after it): each group rescales half of its columns to m_new
                 if (!warp_wait(sm, &sm->bar[kPvDone], (i - 1) & 1, A.status)) { ok = false; break; }
                 fence_after();
                 const float f = need ? ex2(m - m_new) : 1.f;  // m = -inf: O is zero so far
 #pragma unroll 1
-                for (int c0 = 0; c0 < kHalfV; c0 += 32) {
+                for (int c0 = (kHalfV / 2) * grp; c0 < (kHalfV / 2) * (grp + 1); c0 += 32) {
                     uint32_t o[32];
                     HS_LD32(o, tmem + lrow + kColO + c0);
                     tmem_wait_ld();
@@ -468,9 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
                 l *= f;
             }
             m = m_new;
-            // pass 2: P = 2^(x - m) in bf16, written over the scores already read
+            // pass 2: P = 2^(x - m) in bf16, written over this group's scores already read
 #pragma unroll 1
-            for (int ch = 0; ch < kBlk / 32; ++ch) {
+            for (int ch = 4 * grp; ch < 4 * grp + 4; ++ch) {
                 uint32_t r[32];
                 HS_LD32(r, tmem + lrow + kColS + 32 * ch);
                 tmem_wait_ld();
@@ -485,12 +501,17 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
                     l += pr.x + pr.y;
                     pk[c] = *reinterpret_cast<const uint32_t*>(&pb);
                 }
-                HS_ST16(tmem + lrow + kColS + 16 * ch, pk);
+                HS_ST16(tmem + lrow + kColS + 16 * ch + 64 * grp, pk);
             }
             tmem_wait_st();
             fence_before();
             bar_arrive(&sm->bar[kPFull]);
         }
+        // the running sum is the two groups' parts
+        sm->lsum[grp][h] = l;
+        bar_arrive(&sm->bar[kLsum]);
+        if (ok && !warp_wait(sm, &sm->bar[kLsum], 0, A.status)) ok = false;
+        l = sm->lsum[0][h] + sm->lsum[1][h];
         if (ok && nb > 0 && warp_wait(sm, &sm->bar[kPvDone], (nb - 1) & 1, A.status)) {
             fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -499,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
             else orow = (((size_t)b * A.nsplit + split) * A.H + h) * kDimV;
             float* dst = A.o + orow + kHalfV * v;
 #pragma unroll 1
-            for (int c0 = 0; c0 < kHalfV; c0 += 32) {
+            for (int c0 = (kHalfV / 2) * grp; c0 < (kHalfV / 2) * (grp + 1); c0 += 32) {
                 uint32_t o[32];
                 HS_LD32(o, tmem + lrow + kColO + c0);
                 tmem_wait_ld();
@@ -511,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
                                         __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
                 }
             }
-            if (v == 0 && h < A.H) {
+            if (v == 0 && grp == 0 && h < A.H) {
                 const float lse = l > 0.f ? (m + lg2(l)) * 0.69314718055994531f : -INFINITY;
                 if (A.nsplit == 1) A.lse[(size_t)b * A.H + h] = lse;
                 else A.lse[((size_t)b * A.nsplit + split) * A.H + h] = lse;
@@ -519,8 +540,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
         } else if (ok && nb == 0 && h < A.H) {  // no keys in this split
             size_t orow = A.nsplit == 1 ? ((size_t)b * A.H + h) * kDimV
                                         : (((size_t)b * A.nsplit + split) * A.H + h) * kDimV;
-            for (int d = 0; d < kHalfV; ++d) A.o[orow + kHalfV * v + d] = 0.f;
-            if (v == 0) {
+            for (int d = (kHalfV / 2) * grp; d < (kHalfV / 2) * (grp + 1); ++d) A.o[orow + kHalfV * v + d] = 0.f;
+            if (v == 0 && grp == 0) {
                 if (A.nsplit == 1) A.lse[(size_t)b * A.H + h] = -INFINITY;
                 else A.lse[((size_t)b * A.nsplit + split) * A.H + h] = -INFINITY;
             }
