@@ -10,22 +10,24 @@
 // R^576, value V_j = latent_j in R^512, per head s_hj = sm_scale * <q_h, K_j> over the
 // selections whose slot is valid, o_h = softmax(s_h) V, lse_h = ln sum_j exp(s_hj).
 //
-// attend_kernel: one CTA per (request b, key split s, value half v), 416 threads, one CTA
-// per SM (222 KB of shared memory, 512 TMEM columns).
+// attend_kernel: one CTA per (request b, key split s, value half v), 800 threads, one CTA
+// per SM (225 KB of shared memory, 512 TMEM columns).
 //   * Q [128 heads x 576] bf16 stays in shared memory for the whole CTA, in the 128-byte
 //     swizzled K-major layout the MMA reads (heads beyond H are zero rows).
-//   * 8 producer warps gather blocks of 32 selected entries through out_slots (one key
-//     per lane, one 64-dimension slice per warp), decode the E4M3 codes times their
-//     block scale to bf16 and store them swizzled into one of two stages: the stage is
-//     K (K-major, 576 wide) for S = Q K^T and, read MN-major, V (256 wide, this CTA's
-//     half) for O += P V -- one copy serves both products.
-//   * one thread issues the MMAs: S (M=128 heads, N=32 keys, K=576) into TMEM, and
-//     O += P V (M=128, N=256, K=32) with P read from TMEM; completion is signalled
-//     through mbarriers by tcgen05.commit.
-//   * 4 softmax warps (thread = head = TMEM lane) read S, keep a running maximum m (log2
-//     domain) that moves only when a block's maximum exceeds it by more than 8 -- then O
-//     (in TMEM) and the running sum are rescaled -- and write P = 2^(x - m) as bf16 into
-//     TMEM; at the end they normalise O and write it with lse.
+//   * Keys come in blocks of 256 selections. 16 producer warps gather their rows through
+//     out_slots, decode the E4M3 codes times their block scale to bf16 and fill two 32 KB
+//     stages: per block nine K chunks (256 keys x 64 dims, K-major) and four V chunks
+//     (64 keys x this CTA's 256 value dims, read MN-major).
+//   * one thread issues the MMAs: S = Q K^T (M=128 heads, N=256 keys, K=16 per
+//     instruction, 36 per block) into 256 TMEM columns, and O += P V (M=128, N=256 value
+//     dims, K=16 keys, 16 per block) with P read from TMEM; completion is signalled through
+//     mbarriers by tcgen05.commit. The widest N keeps the tensor core busy: an M=128
+//     instruction costs about the same whatever N is.
+//   * 8 softmax warps in two groups of 128 keys (thread = head = TMEM lane in both) read
+//     S, keep a running maximum m (log2 domain) that moves only when a block's maximum
+//     exceeds it by more than 8 -- then O (in TMEM) and the running sums are rescaled --
+//     and write P = 2^(x - m) as bf16 over the scores already read; at the end they
+//     normalise O and write it with lse.
 // With several key splits per request each CTA writes its normalised partial and its
 // lse; combine_kernel merges them (weights exp(lse_s - lse)).
 //
