@@ -623,7 +623,7 @@ __device__ __forceinline__ void fetch_request(const Layout& L, const int32_t* ou
     if (threadIdx.x == 0) *count = ready;
 }
 
-__global__ void __launch_bounds__(kGatherThreads, kGatherCtasPerSm)
+__global__ void __launch_bounds__(kGatherThreads, 2)  // <= 64 registers: fits beside a resolution CTA
 gather_kernel(const Layout L, const int32_t* __restrict__ out, int k, int sync) {
     __shared__ uint32_t bcast[2];
     const uint32_t G = gridDim.x, c = blockIdx.x, R = (uint32_t)L.R;
