@@ -107,6 +107,7 @@ def resolved_context(w, T, B):
     (3, 200, 64, 256),     # ragged last block, fewer heads
     (80, 96, 16, 128),     # one split per request (B x 2 CTAs >= SMs)
     (1, 33, 1, 64),        # one head, one key past a block
+    (1, 5000, 32, 6000),   # more selections than one CTA stages: at least three key splits
 ])
 def test_attend_matches_oracle_after_resolution(B, k, H, S):
     w = tracegen.Workload("att", 11, B=B, L=1, C=4 * S, S=S, k=k, E=656, kv_kind=tracegen.KV_DSA656,

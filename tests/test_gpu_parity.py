@@ -130,6 +130,7 @@ def test_noio_all_hits_after_first_call():
     (300, 33, 7, 48, 2),       # S not a multiple of 32
     (2049, 2047, 2047, 32, 2), # k = S just below a power of two, C ragged past a group
     (100000, 777, 513, 144, 5),
+    (20000, 6000, 5000, 32, 2),  # k above one probe batch of 4 x 512: batched probe and re-read answers
 ])
 def test_random_shapes_and_ragged_tails(C, S, k, E, B):
     w = tracegen.Workload("ragged", 9, B=B, L=1, C=C, S=S, k=k, E=E, kv_kind=tracegen.KV_RAW,
