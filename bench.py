@@ -300,6 +300,11 @@ def run_ours(args, rank: int, world: int, dist) -> None:
             ctx.resolve_host(sel_pin[t].numpy(), out_np, miss_np)
             e2e_s += time.perf_counter() - t0
 
+        # ---- the same steps back to back in one CUDA graph (warm L2, as in a decode graph)
+        graph = None
+        if not args.no_extras and rank == 0:
+            graph = measure_graph(torch, ctx, w, sel_dev, out_dev, miss_dev, W, K)
+
         # ---- the same steps through a pooled context (requests' histories at permuted extents
         # of one shared pinned store)
         pooled = None
@@ -390,6 +395,7 @@ def run_ours(args, rank: int, world: int, dist) -> None:
         "kernels": kernels,
         "no_io": noio,
         "append": append,
+        "graph": graph,
         "pooled": pooled,
         "policies": policies,
         "attend": attend,
@@ -564,6 +570,34 @@ def measure_policies(torch, hs, ctx, w, sel_dev, out_dev, miss_dev, flush, W: in
         curve[str(S)] = row
     return {"step": step, "misses_per_step_by_slots": curve, "trace_steps_for_curve": T,
             "seed": POLICY_SEED}
+
+
+def measure_graph(torch, ctx, w, sel_dev, out_dev, miss_dev, W: int, K: int) -> dict:
+    """Steps W..W+K-1 captured in one CUDA graph after the W warm-up steps and replayed once:
+    µs per layer-step as a decode graph sees it (no flush between steps; every step is a
+    distinct selection, so the state advances as it does eagerly)."""
+    ctx.reset()
+    for t in range(W):
+        ctx.resolve(sel_dev[t], out_dev[t], miss_dev[t])
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(K):
+                ctx.resolve(sel_dev[W + i], out_dev[W + i], miss_dev[W + i], stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    g.replay()
+    b.record()
+    b.synchronize()
+    us = a.elapsed_time(b) * 1e3 / K
+    misses = float(miss_dev[W:W + K].sum()) / K
+    return {"us_per_layer_step": us, "resolutions_per_s": w.B / (us * 1e-6), "steps": K,
+            "misses_per_step": misses, "miss_fetch_gbs": misses * w.E / (us * 1e-6) / 1e9,
+            "how": "one replay of a graph holding the K timed steps, after the W warm-up steps eagerly"}
 
 
 def measure_pooled(torch, hs, ctx, w, sel_dev, out_dev, miss_dev, flush, W: int, K: int) -> dict:
