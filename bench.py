@@ -55,23 +55,33 @@ def workload_for_rank(name: str, rank: int):
     return w if rank == 0 else replace(w, seed=w.seed + 7919 * rank)
 
 
+def kernel_code_digest(path: str) -> str:
+    """sha256 of a CUDA source with its comments and whitespace removed: it changes when
+    the code changes, not when a comment does."""
+    import hashlib
+    import re
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return hashlib.sha256("".join(text.split()).encode()).hexdigest()
+
+
 def profiled_traffic(kernel: str, workload: str):
     """ncu figures recorded in profiles/<kernel>_<workload>.md, or None once the kernel
-    source has changed since the capture (its sha256 is recorded beside them)."""
-    import hashlib
+    code has changed since the capture (its digest is recorded beside them)."""
     import re
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     src = os.path.join(ROOT, "hierarchical_kv_cache_swap_gb300", "csrc", "hs_kernels.cu")
     try:
         text = open(path).read()
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        digest = kernel_code_digest(src)
     except OSError:
         return None
     m = re.search(r"```json\n(.*?)```", text, re.S)
     if not m:
         return None
     fig = json.loads(m.group(1))
-    return fig if fig.get("kernel_source_sha256") == digest else None
+    return fig if fig.get("kernel_code_sha256") == digest else None
 
 
 def reduce_max(values, dist, device):

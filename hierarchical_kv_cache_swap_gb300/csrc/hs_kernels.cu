@@ -22,8 +22,9 @@
 //      pair the r-th miss with the r-th victim and answer the missed selections; the
 //      answers name every row's slot, so they are PUBLISHED (ready_slot) before the
 //      page table, slot tokens and stamps are updated.
-// gather_kernel -- a persistent grid of 2 CTAs per SM, launched right behind the
-//   resolution (PDL) so that it is resident while the resolution runs. Each CTA owns
+// gather_kernel -- a persistent grid of one CTA per SM (held to 64 registers, so that it
+//   fits beside a resolution CTA), launched right behind the resolution (PDL) so that it
+//   is resident while the resolution runs. Each CTA owns
 //   a share of one request's fetch list: it waits for ready_pos, issues the 16-byte
 //   zero-copy loads of its rows from the mapped host store (coalesced, 8 in flight
 //   per thread), waits for ready_slot only when it has to store, and writes each row
