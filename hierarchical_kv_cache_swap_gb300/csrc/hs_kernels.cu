@@ -56,6 +56,10 @@ namespace {
 constexpr int NT = kResolveThreads;
 constexpr int NW = kResolveWarps;
 
+__device__ __forceinline__ void pdl_wait_prerequisites() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -518,6 +522,9 @@ __global__ void __launch_bounds__(kResolveThreads, 2)
 resolve_kernel(const Layout L, const int32_t* __restrict__ sel, int k, int32_t* __restrict__ out,
                int32_t* __restrict__ miss_counts, int fetch) {
     extern __shared__ __align__(16) uint8_t smem[];
+    // Launched as a programmatic dependent of the previous call's fetch grid: nothing is
+    // read before that grid (and, through its own wait, the previous resolution) is done.
+    pdl_wait_prerequisites();
     pdl_launch_dependents();  // the fetch grid may start now; it synchronizes per request
     const int b = blockIdx.x;
     const Plan P(L.C, L.S);
@@ -627,6 +634,9 @@ __device__ __forceinline__ void fetch_request(const Layout& L, const int32_t* ou
 __global__ void __launch_bounds__(kGatherThreads, 2)  // <= 64 registers: fits beside a resolution CTA
 gather_kernel(const Layout L, const int32_t* __restrict__ out, int k, int sync) {
     __shared__ uint32_t bcast[2];
+    // The next call's resolution may be scheduled once every fetch CTA is resident (it
+    // waits for this grid to finish before it reads anything).
+    pdl_launch_dependents();
     const uint32_t G = gridDim.x, c = blockIdx.x, R = (uint32_t)L.R;
     if (G >= R) {  // several CTAs share each request
         const uint32_t b = c % R;
@@ -634,6 +644,9 @@ gather_kernel(const Layout L, const int32_t* __restrict__ out, int k, int sync) 
     } else {  // each CTA takes whole requests
         for (uint32_t b = c; b < R; b += G) fetch_request(L, out, k, (int)b, 0, 1, sync != 0, bcast);
     }
+    // This grid ends only after the resolution it serves: a successor that waits for this
+    // grid then also sees every table update of that resolution.
+    pdl_wait_prerequisites();
 }
 
 }  // namespace
@@ -675,9 +688,20 @@ cudaError_t configure_kernels(int device) {
 
 cudaError_t launch_resolve(const Layout& L, cudaStream_t stream, const int32_t* sel, int k,
                            int32_t* out_slots, int32_t* miss_counts, bool fetch) {
-    resolve_kernel<<<L.R, kResolveThreads, resolve_smem_bytes(L.C, L.S), stream>>>(L, sel, k, out_slots,
-                                                                                   miss_counts, fetch ? 1 : 0);
-    return cudaGetLastError();
+    // a programmatic dependent of whatever precedes it on the stream: it is scheduled early
+    // only behind a grid that allows it (the previous call's fetch), and waits for that
+    // grid's completion before its first read
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)L.R);
+    cfg.blockDim = dim3(kResolveThreads);
+    cfg.dynamicSmemBytes = resolve_smem_bytes(L.C, L.S);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, resolve_kernel, L, sel, k, out_slots, miss_counts, fetch ? 1 : 0);
 }
 
 cudaError_t launch_gather(const Layout& L, cudaStream_t stream, const int32_t* out_slots, int k, int num_sms,
