@@ -242,10 +242,12 @@ struct Request {
         sb = reinterpret_cast<uint16_t*>(smem + P.sb);
     }
 
-    // Starts the asynchronous copy of the request's last-use stamps into keys[] (they
-    // are only needed to rank victims, and arrive while the page table is probed) and
-    // clears the bitmaps; no barrier. Every exit path must wait for the copy (drain()).
-    __device__ void start() {
+    // Starts the asynchronous copy of the request's last-use stamps into keys[]: they
+    // are only needed to rank victims, so the copy starts once the probe has found a miss
+    // and lands while the misses are ranked (a call without a miss never reads them). A
+    // hit slot's stamp may be copied before or after the probe restamped it; hit slots
+    // are never candidates. Every exit path after it waits for it (drain()).
+    __device__ void prefetch_stamps() {
         const int tid = threadIdx.x;
         const int S = L.S;
         if ((S & 3) == 0 && ((uintptr_t)lub & 15) == 0) {  // 16-byte chunks when aligned
@@ -254,6 +256,11 @@ struct Request {
             for (int i = tid; i < S; i += NT) cp_async4(keys + i, lub + i);
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+
+    // Clears the bitmaps and counters; no barrier.
+    __device__ void start() {
+        const int tid = threadIdx.x;
         for (int i = tid; i < P.CW; i += NT) posbm[i] = 0u;
         for (int i = tid; i < P.SW; i += NT) hitbm[i] = 0u;
         if (tid == 0) {
@@ -378,7 +385,7 @@ struct Request {
     // stamp + 1 (LRU: last use, FIFO: fill call) or the RANDOM policy's draw; sets victims.
     __device__ void rank_victims() {
         const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-        drain();  // the stamps copied at kernel start have landed (this thread's part) ...
+        drain();  // the stamps copied after the probe have landed (this thread's part) ...
         __syncthreads();  // ... and everyone's
         const bool drawn = L.policy == kPolicyRandom;
         const uint64_t stream = drawn ? splitmix64(L.seed, (uint64_t)b) : 0ull;
@@ -564,6 +571,7 @@ resolve_kernel(const Layout L, const int32_t* __restrict__ sel, int k, int32_t* 
     // The fetch list is complete (the probe ended with a barrier, and the release is
     // cumulative over it): the fetch of this request's rows can start now.
     if (pub && threadIdx.x == 0) st_release(rpos, tag | R.scratch[2 * NW + 2]);
+    R.prefetch_stamps();
     R.rank_misses();
     R.rank_victims();
     R.answer_misses(p);
