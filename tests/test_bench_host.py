@@ -59,3 +59,17 @@ def test_weak_scaling_value_counts_every_rank():
     assert bench.weak_scaling_value(1, 32, 10, 1000.0) == pytest.approx(320.0)
     assert bench.weak_scaling_value(4, 32, 10, 1000.0) == pytest.approx(1280.0)
     assert bench.reduce_max([1, 2], None, "cpu") == [1.0, 2.0]
+
+
+def test_kernel_code_digest_ignores_comments_only(tmp_path):
+    """The profile figures are keyed to the kernel code: a comment or whitespace edit keeps
+    the key, a code edit changes it."""
+    import bench
+    a = tmp_path / "a.cu"
+    a.write_text("// header\n__global__ void k(int* p) { /* note */ p[0] = 1; }\n")
+    b = tmp_path / "b.cu"
+    b.write_text("// another header\n\n__global__ void k(int* p) {\n    p[0] = 1;  // same code\n}\n")
+    c = tmp_path / "c.cu"
+    c.write_text("__global__ void k(int* p) { p[0] = 2; }\n")
+    assert bench.kernel_code_digest(str(a)) == bench.kernel_code_digest(str(b))
+    assert bench.kernel_code_digest(str(a)) != bench.kernel_code_digest(str(c))
