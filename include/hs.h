@@ -326,7 +326,9 @@ hs_ctx* hs_create_pooled(int num_requests, int context_len, int slots, int entry
  * arrays base[R] >= 0, len[R] in [0, context_len], base + len <= pool_rows). Every request
  * whose extent changes is a new request: its cache state (page table, slots, stamps,
  * call counter, slot contents) is emptied. Enqueued on `stream` (copies from the caller's
- * arrays, which may be reused on return). Returns HS_OK, HS_ERR_INVALID or HS_ERR_CUDA.
+ * arrays, which may be reused on return); an admission-time call, not meant to be
+ * captured into a CUDA graph (its copies come from pageable memory). Returns HS_OK,
+ * HS_ERR_INVALID or HS_ERR_CUDA.
  */
 int hs_set_extents(hs_ctx* ctx, hs_stream_t stream, const int64_t* base, const int32_t* len);
 
