@@ -73,3 +73,26 @@ def test_kernel_code_digest_ignores_comments_only(tmp_path):
     c.write_text("__global__ void k(int* p) { p[0] = 2; }\n")
     assert bench.kernel_code_digest(str(a)) == bench.kernel_code_digest(str(b))
     assert bench.kernel_code_digest(str(a)) != bench.kernel_code_digest(str(c))
+
+
+def test_reference_arm_under_two_ranks_prints_one_line():
+    """`bench.py --impl reference` launched as the driver launches it for N = 2: one JSON
+    line from rank 0 with the reference arm's keys, the other rank exits 0 without output."""
+    import json
+    import subprocess
+    import sys
+    import oracle
+    import tracegen
+    oracle.build()
+    tracegen.build()
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "1", "--workload", "tiny"]
+    res = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
