@@ -23,12 +23,14 @@
  * table, slot tokens and last use at -1, step 0, device buffer zero.
  *
  * Replacement rule (the pages leave the order open; this is the deterministic
- * reading implemented): in a call with stamp t, slots hit by the selection are
+ * reading implemented, HS_POLICY_LRU, the default; hs_set_policy selects the FIFO and
+ * random comparison policies): in a call with stamp t, slots hit by the selection are
  * stamped t and are not evictable; the distinct missed positions, in ascending
  * order, take in order the non-hit slots with the smallest (last_use, slot index);
  * the position a victim held is unmapped, the new one mapped and stamped t, and its
  * host row copied into the slot. A negative selection is padding (slot -1, neither
- * hit nor miss); a selection >= C yields slot -1 and sets HS_STATUS_RANGE; a position
+ * hit nor miss); a selection >= C (in a pooled context, >= the request's extent
+ * length) yields slot -1 and sets HS_STATUS_RANGE; a position
  * repeated within one row resolves to the same slot each time, counts once, and sets
  * HS_STATUS_DUP.
  *
