@@ -13,6 +13,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <new>
+
 #include "hs.h"
 #include "hs_internal.h"
 
@@ -68,7 +70,7 @@ void free_ctx(hs_ctx* h) {
     cudaFree(h->d_len);
     free(h->ext_base);
     free(h->ext_len);
-    free(h);
+    delete h;
 }
 
 int check_call(hs_ctx* h, const void* sel, int B, int k, const void* out, const void* miss) {
@@ -160,7 +162,7 @@ hs_ctx* create(int num_requests, int context_len, int slots, int entry_bytes, ui
         return nullptr;
     }
 
-    hs_ctx* h = (hs_ctx*)calloc(1, sizeof(hs_ctx));
+    hs_ctx* h = new (std::nothrow) hs_ctx();  // value-initialised: every member zero
     if (!h) {
         fail(HS_ERR_NOMEM, "out of host memory");
         return nullptr;

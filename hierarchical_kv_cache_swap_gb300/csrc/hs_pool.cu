@@ -49,14 +49,17 @@ void hs_pool_destroy(hs_pool* p) { delete p; }
 
 int64_t hs_pool_reserve(hs_pool* p, int64_t n) {
     if (!p || n <= 0) return -1;
-    for (auto it = p->free.begin(); it != p->free.end(); ++it) {
-        if (it->second < n) continue;
-        const int64_t base = it->first, len = it->second;
-        p->free.erase(it);
-        if (len > n) p->free[base + n] = len - n;
-        p->used[base] = n;
-        p->free_rows -= n;
-        return base;
+    try {  // no exception crosses the C ABI: out of memory reads as "no extent"
+        for (auto it = p->free.begin(); it != p->free.end(); ++it) {
+            if (it->second < n) continue;
+            const int64_t base = it->first, len = it->second;
+            p->used[base] = n;  // first: if this throws, nothing has changed
+            p->free.erase(it);
+            if (len > n) p->free[base + n] = len - n;
+            p->free_rows -= n;
+            return base;
+        }
+    } catch (...) {
     }
     return -1;
 }
@@ -65,23 +68,31 @@ int hs_pool_release(hs_pool* p, int64_t base) {
     if (!p) return HS_ERR_INVALID;
     auto u = p->used.find(base);
     if (u == p->used.end()) return HS_ERR_INVALID;
-    int64_t b = base, n = u->second;
-    p->used.erase(u);
-    p->free_rows += n;
-    auto next = p->free.lower_bound(b);
-    if (next != p->free.end() && next->first == b + n) {  // merge with the following free extent
-        n += next->second;
-        next = p->free.erase(next);
+    // find the free neighbours first and insert the merged extent before erasing anything,
+    // so that an allocation failure (the one insertion) leaves the pool as it was
+    const int64_t n0 = u->second;
+    auto next = p->free.lower_bound(base);
+    const bool merge_next = next != p->free.end() && next->first == base + n0;
+    auto prev = next;
+    bool merge_prev = false;
+    if (next != p->free.begin()) {
+        prev = std::prev(next);
+        merge_prev = prev->first + prev->second == base;
     }
-    if (next != p->free.begin()) {  // and with the preceding one
-        auto prev = std::prev(next);
-        if (prev->first + prev->second == b) {
-            b = prev->first;
-            n += prev->second;
-            p->free.erase(prev);
+    const int64_t b = merge_prev ? prev->first : base;
+    const int64_t n = (merge_prev ? prev->second : 0) + n0 + (merge_next ? next->second : 0);
+    if (merge_prev) {
+        prev->second = n;  // grows in place: no allocation
+    } else {
+        try {
+            p->free[b] = n;
+        } catch (...) {
+            return HS_ERR_NOMEM;
         }
     }
-    p->free[b] = n;
+    if (merge_next) p->free.erase(next);
+    p->used.erase(u);
+    p->free_rows += n0;
     return HS_OK;
 }
 

@@ -299,9 +299,10 @@ int hs_plan(const hs_plan_params* in, hs_plan_result* out);
  * finishes (merged with free neighbours). The pool only does the bookkeeping; the rows
  * themselves are a pinned, mapped store the caller allocates (see hs_create_pooled).
  *   hs_pool_create   NULL if rows <= 0 or out of memory; hs_pool_destroy frees it.
- *   hs_pool_reserve  base row of a new extent of n > 0 rows, or -1 if none is long enough.
- *   hs_pool_release  frees the extent reserved at `base`: HS_OK, or HS_ERR_INVALID if no
- *                    extent starts there.
+ *   hs_pool_reserve  base row of a new extent of n > 0 rows, or -1 if none is long enough
+ *                    (or the bookkeeping could not allocate).
+ *   hs_pool_release  frees the extent reserved at `base`: HS_OK, HS_ERR_INVALID if no
+ *                    extent starts there, or HS_ERR_NOMEM (the pool is left unchanged).
  *   hs_pool_free_rows, hs_pool_largest_free   free rows in total, and in one extent.
  */
 typedef struct hs_pool hs_pool;
