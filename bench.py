@@ -181,7 +181,8 @@ def resolve_hbm_bytes(w, miss) -> float:
 
     Per request: selections 4k, page-table probes 4k, hit stamps 4h, output 4k, and when
     there are misses a scan of the S last-use stamps 4S, slot-token reads 4m, page-table
-    unmap + map 8m, stamps 4m, miss list 8m, plus the counters.
+    unmap + map 8m, stamps 4m, miss list 8m, the fetch's device copy of the answers 4m,
+    plus the counters.
     """
     total = 0
     for m in miss:
@@ -189,7 +190,7 @@ def resolve_hbm_bytes(w, miss) -> float:
         h = w.k - m
         b = 12 * w.k + 4 * h + 12
         if m:
-            b += 4 * w.S + 24 * m
+            b += 4 * w.S + 28 * m
         total += b
     return float(total)
 
@@ -415,7 +416,8 @@ def run_ours(args, rank: int, world: int, dist) -> None:
         "clocks": clocks,
         "e2e": {"value": weak_scaling_value(world, w.B, K, e2e_s * 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": w.B * w.k * 4, "d2h_bytes_per_step": w.B * w.k * 4 + w.B * 4,
-                "how": "hs_resolve_host: pinned selections in, out_slots + miss_counts out, stream sync"},
+                "how": "hs_resolve_host with page-locked buffers: the kernels read the selections and "
+                       "write out_slots + miss_counts in host memory in place; stream sync"},
         "wall_s_timed_region": wall,
     }
     if not args.no_extras:

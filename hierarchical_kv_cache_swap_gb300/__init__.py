@@ -251,8 +251,15 @@ class Context:
 
     def resolve_host(self, selections: np.ndarray, out_slots: np.ndarray, miss_counts: np.ndarray,
                      stream=None) -> None:
-        """Resolve with host buffers (copies in, resolves, copies out, waits)."""
+        """Resolve with host numpy buffers and wait. Page-locked buffers (e.g. views of
+        pinned torch tensors) are accessed by the kernels in place; pageable ones are staged
+        through device buffers."""
+        for a in (selections, out_slots, miss_counts):
+            if not (isinstance(a, np.ndarray) and a.dtype == np.int32 and a.flags.c_contiguous):
+                raise ValueError("resolve_host wants C-contiguous int32 numpy arrays")
         B, k = selections.shape
+        if out_slots.shape != (B, k) or miss_counts.shape != (B,):
+            raise ValueError(f"out_slots must be {(B, k)} and miss_counts {(B,)}")
         self._check(self._lib.hs_resolve_host(self._h, _stream(stream), _addr(selections), B, k,
                                               _addr(out_slots), _addr(miss_counts)),
                     "hs_resolve_host")

@@ -66,11 +66,25 @@ void free_ctx(hs_ctx* h) {
     cudaFree(h->stage_sel);
     cudaFree(h->stage_out);
     cudaFree(h->stage_miss);
+    cudaFree(h->L.jslot);
     cudaFree(h->d_base);
     cudaFree(h->d_len);
     free(h->ext_base);
     free(h->ext_len);
     delete h;
+}
+
+// The device address of a host buffer that kernels may access in place: page-locked
+// memory mapped into the device's address space, 4-byte aligned. nullptr for pageable
+// memory, device memory or anything the runtime does not know.
+void* in_place(const void* p) {
+    if ((reinterpret_cast<uintptr_t>(p) & 3u) != 0) return nullptr;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();  // not a pointer the runtime knows: clear the error it set
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
 }
 
 int check_call(hs_ctx* h, const void* sel, int B, int k, const void* out, const void* miss) {
@@ -213,6 +227,7 @@ hs_ctx* create(int num_requests, int context_len, int slots, int entry_bytes, ui
     HS_ALLOC(h->stage_sel, sizeof(int32_t) * (size_t)R * S);
     HS_ALLOC(h->stage_out, sizeof(int32_t) * (size_t)R * S);
     HS_ALLOC(h->stage_miss, sizeof(int32_t) * (size_t)R);
+    HS_ALLOC(L.jslot, sizeof(int32_t) * (size_t)R * S);
     if (pool_rows > 0) {
         h->pool_rows = pool_rows;
         HS_ALLOC(h->d_base, sizeof(int64_t) * (size_t)R);
@@ -427,14 +442,23 @@ int hs_resolve_host(hs_ctx* h, hs_stream_t stream, const int32_t* sel_host, int 
     cudaStream_t s = (cudaStream_t)stream;
     const size_t n = sizeof(int32_t) * (size_t)B * k;
     cudaError_t e;
-    if ((e = cudaMemcpyAsync(h->stage_sel, sel_host, n, cudaMemcpyHostToDevice, s)) != cudaSuccess)
-        return cuda_fail(e, "selections host->device");
-    rc = enqueue(h, s, h->stage_sel, k, h->stage_out, h->stage_miss, nullptr);
+    // Page-locked buffers are read and written by the kernels in place (over the
+    // host link); pageable ones go through the context's device staging buffers.
+    const int32_t* dsel = static_cast<const int32_t*>(in_place(sel_host));
+    int32_t* dout = static_cast<int32_t*>(in_place(out_host));
+    int32_t* dmiss = static_cast<int32_t*>(in_place(miss_host));
+    if (!dsel) {
+        if ((e = cudaMemcpyAsync(h->stage_sel, sel_host, n, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+            return cuda_fail(e, "selections host->device");
+        dsel = h->stage_sel;
+    }
+    rc = enqueue(h, s, dsel, k, dout ? dout : h->stage_out, dmiss ? dmiss : h->stage_miss, nullptr);
     if (rc != HS_OK) return rc;
-    if ((e = cudaMemcpyAsync(out_host, h->stage_out, n, cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(miss_host, h->stage_miss, sizeof(int32_t) * (size_t)B, cudaMemcpyDeviceToHost,
-                             s)) != cudaSuccess)
-        return cuda_fail(e, "results device->host");
+    if (!dout && (e = cudaMemcpyAsync(out_host, h->stage_out, n, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_fail(e, "out_slots device->host");
+    if (!dmiss && (e = cudaMemcpyAsync(miss_host, h->stage_miss, sizeof(int32_t) * (size_t)B,
+                                       cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_fail(e, "miss_counts device->host");
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     return HS_OK;
 }

@@ -48,6 +48,9 @@ struct Layout {
     uint32_t* gcount;      // [R + G]: fetch CTA counters; (b, share q) at b + q*R; tag = gcount[b] + 1
     const int64_t* row_base = nullptr;  // [R] pooled store: first row of request b (else b * C)
     const int32_t* row_len = nullptr;   // [R] pooled store: positions request b has (else C)
+    // [R][k] device copy of the slots given to missed selections, which the fetch reads;
+    // null: the fetch reads them from out_slots (which must then be device memory)
+    int32_t* jslot = nullptr;
     int policy = kPolicyLru;  // replacement policy of the calls launched with this layout
     uint64_t seed = 0;        // kPolicyRandom's seed
 };

@@ -501,7 +501,9 @@ struct Request {
         uint32_t rank = gprefix[g];
         for (int q = g * kGroupWords; q < w; ++q) rank += __popc(posbm[q]);
         rank += __popc(word & (bit - 1u));
-        outb[j] = victims[rank];
+        const int32_t v = victims[rank];
+        outb[j] = v;
+        if (L.jslot) L.jslot[(size_t)b * k + j] = v;  // the fetch's copy, in device memory
     }
 
     // p: the selections this thread probed in the first batch (still in registers).
@@ -597,7 +599,7 @@ __device__ __forceinline__ void fetch_rows(const Layout& L, const int32_t* out, 
     const uint32_t n = rows * cpr;
     const int32_t* gpos = L.fpos + (size_t)b * L.S;
     const int32_t* gsel = L.fsel + (size_t)b * L.S;
-    const int32_t* ob = out + (size_t)b * k;
+    const int32_t* ob = (L.jslot ? L.jslot : out) + (size_t)b * k;
     const uint8_t* hb = L.host + (size_t)(L.row_base ? __ldg(L.row_base + b) : (int64_t)b * L.C) * L.host_stride;
     uint8_t* db = L.dev + (size_t)b * L.S * L.E;
     bool slots_known = false;

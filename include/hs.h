@@ -120,11 +120,12 @@ int hs_resolve(hs_ctx* ctx, hs_stream_t stream, const int32_t* selections, int B
                int32_t* out_slots, int32_t* miss_counts);
 
 /*
- * hs_resolve_host -- hs_resolve with HOST buffers: copies selections host->device,
- * resolves, copies out_slots and miss_counts device->host, and waits for the stream.
- * Buffers may be pageable or pinned (pinned is faster). Staging buffers are
- * preallocated by hs_create. Same arguments and errors as hs_resolve; returns after
- * the results are in the host buffers.
+ * hs_resolve_host -- hs_resolve with HOST buffers; returns after the results are in
+ * them (it waits for the stream). A page-locked buffer (cudaHostAlloc, cudaMallocHost,
+ * or cudaHostRegister'ed and mapped; 4-byte aligned) is read or written by the kernels
+ * in place over the host link, with no copy; any other host buffer (pageable memory) is
+ * staged through device buffers preallocated by hs_create, with one copy each way. The
+ * three buffers are classified independently. Same arguments and errors as hs_resolve.
  */
 int hs_resolve_host(hs_ctx* ctx, hs_stream_t stream, const int32_t* selections_host, int B, int k,
                     int32_t* out_slots_host, int32_t* miss_counts_host);

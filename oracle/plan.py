@@ -13,9 +13,10 @@ def plan(top_k, device_buffer_size, host_to_device_ratio, entry_bytes, layers, c
     S, C, L, E = device_buffer_size, context_len, layers, entry_bytes
     # one request, one layer: its buffer, its page table over C positions, slot tokens and
     # stamps (4 bytes each per slot), its miss list (position and index, 4 bytes each per
-    # slot), the host-call staging (selections and answers, 4 bytes each per slot) and 16
-    # bytes of counters and flags
-    per_layer = S * E + 4 * C + 4 * S + 4 * S + 8 * S + 8 * S + 16
+    # slot), the device copy of the missed selections' answers that the fetch reads (4 bytes
+    # per slot), the host-call staging (selections and answers, 4 bytes each per slot) and
+    # 16 bytes of counters and flags
+    per_layer = S * E + 4 * C + 4 * S + 4 * S + 8 * S + 4 * S + 8 * S + 16
     device_bytes = L * per_layer
     by_device = hbm_bytes // device_bytes
     rows = min(int(host_to_device_ratio * by_device * S), host_bytes // (E * L))

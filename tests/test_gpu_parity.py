@@ -249,17 +249,27 @@ def test_graph_replay_equals_eager():
     graph.close()
 
 
-def test_host_buffer_entry_point_matches_device_entry_point():
+def _host_buffer(shape, pinned):
+    if pinned:  # page-locked: the kernels read or write it in place
+        return torch.empty(shape, dtype=torch.int32).pin_memory().numpy()
+    return np.empty(shape, dtype=np.int32)  # pageable: staged through device buffers
+
+
+@pytest.mark.parametrize("sel_pinned,out_pinned", [(False, False), (True, True), (True, False), (False, True)])
+def test_host_buffer_entry_point_matches_device_entry_point(sel_pinned, out_pinned):
     w = tracegen.WORKLOADS["dsa"]
     T = 10
     a = GpuRun(w, T, B=4)
     b = hs.Context(4, w.C, w.S, w.E)
     tracegen.fill_kv(b.host_kv_address(), b.host_stride, w, B=4)
-    out = np.empty((4, w.k), dtype=np.int32)
-    miss = np.empty(4, dtype=np.int32)
+    sel = _host_buffer(a.sel.shape, sel_pinned)
+    sel[...] = a.sel
+    out = _host_buffer((4, w.k), out_pinned)
+    miss = _host_buffer((4,), out_pinned)
+    out[...] = -7
     for t in range(T):
         a.step(t)
-        b.resolve_host(a.sel[t], out, miss)
+        b.resolve_host(sel[t], out, miss)
         torch.cuda.synchronize()
         assert np.array_equal(out, a.out_dev[t].cpu().numpy())
         assert np.array_equal(miss, a.miss_dev[t].cpu().numpy())

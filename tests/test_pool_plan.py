@@ -85,18 +85,18 @@ EXAMPLE = dict(top_k=2048, device_buffer_size=6144, host_to_device_ratio=10.0, e
 def test_plan_deployment_example_by_hand():
     """The disaggregated-decode knobs (top_k 2048, buffer 6144, ratio 10), a 61-layer model
     with 656-byte entries, 32k + 8k contexts, 100 GiB of HBM and 1500 GiB of pinned host
-    memory. By hand: per layer 6144*656 + 4*40960 + 24*6144 + 16 = 4,030,464 + 163,840 +
-    147,456 + 16 = 4,341,776 B, so 264,848,336 B per request and floor(107,374,182,400 /
-    264,848,336) = 405 requests by HBM; the pool wants 10*405*6144 = 24,883,200 rows and
-    1500 GiB holds floor(1,610,612,736,000 / (61*656)) = 40,249,218 rows, so 24,883,200
-    rows = floor(607.5) = 607 histories of 40960 positions; 405 requests are admitted."""
+    memory. By hand: per layer 6144*656 + 4*40960 + 28*6144 + 16 = 4,030,464 + 163,840 +
+    172,032 + 16 = 4,366,352 B, so 266,347,472 B per request and floor(107,374,182,400 /
+    266,347,472) = 403 requests by HBM; the pool wants 10*403*6144 = 24,760,320 rows and
+    1500 GiB holds floor(1,610,612,736,000 / (61*656)) = 40,249,218 rows, so 24,760,320
+    rows = floor(604.5) = 604 histories of 40960 positions; 403 requests are admitted."""
     r = hs.plan(**EXAMPLE)
-    assert r["device_bytes_per_request"] == 264_848_336
-    assert r["requests_by_device"] == 405
-    assert r["host_pool_rows"] == 24_883_200
-    assert r["requests_by_host"] == 607
-    assert r["requests"] == 405
-    assert r["miss_bytes_per_step"] == pytest.approx(405 * 61 * 0.06 * 2048 * 656)
+    assert r["device_bytes_per_request"] == 266_347_472
+    assert r["requests_by_device"] == 403
+    assert r["host_pool_rows"] == 24_760_320
+    assert r["requests_by_host"] == 604
+    assert r["requests"] == 403
+    assert r["miss_bytes_per_step"] == pytest.approx(403 * 61 * 0.06 * 2048 * 656)
     assert r["link_us_per_step"] == pytest.approx(r["miss_bytes_per_step"] / 200e3)
 
 
