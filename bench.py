@@ -301,14 +301,14 @@ def run_ours(args, rank: int, world: int, dist) -> None:
         sel_pin = torch.from_numpy(sel).pin_memory()
         out_pin = torch.empty((w.B, w.k), dtype=torch.int32).pin_memory()
         miss_pin = torch.empty(w.B, dtype=torch.int32).pin_memory()
-        out_np, miss_np = out_pin.numpy(), miss_pin.numpy()
+        sel_np, out_np, miss_np = sel_pin.numpy(), out_pin.numpy(), miss_pin.numpy()
         e2e_s = 0.0
         for i in range(K):
             t = W + i
             flush.fill_(i & 0xFF)
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-            ctx.resolve_host(sel_pin[t].numpy(), out_np, miss_np)
+            ctx.resolve_host(sel_np[t], out_np, miss_np)
             e2e_s += time.perf_counter() - t0
 
         # ---- the same steps back to back in one CUDA graph (warm L2, as in a decode graph)

@@ -121,6 +121,9 @@ def last_error() -> str:
     return (load_library().hs_last_error() or b"").decode()
 
 
+_I32 = np.dtype(np.int32)
+
+
 def _addr(x) -> int:
     """Device or host address of a torch tensor / numpy array / int."""
     if x is None:
@@ -128,6 +131,8 @@ def _addr(x) -> int:
     if isinstance(x, int):
         return x
     if isinstance(x, np.ndarray):
+        if x.flags.writeable and x.flags.c_contiguous and x.nbytes:
+            return ctypes.addressof(ctypes.c_char.from_buffer(x))  # ~3x cheaper than .ctypes
         return x.ctypes.data
     return x.data_ptr()
 
@@ -255,7 +260,7 @@ class Context:
         pinned torch tensors) are accessed by the kernels in place; pageable ones are staged
         through device buffers."""
         for a in (selections, out_slots, miss_counts):
-            if not (isinstance(a, np.ndarray) and a.dtype == np.int32 and a.flags.c_contiguous):
+            if not isinstance(a, np.ndarray) or a.dtype != _I32 or not a.flags.c_contiguous:
                 raise ValueError("resolve_host wants C-contiguous int32 numpy arrays")
         B, k = selections.shape
         if out_slots.shape != (B, k) or miss_counts.shape != (B,):

@@ -5,6 +5,7 @@ These run without a GPU: only argument checks that return before any CUDA call.
 import os
 import re
 
+import numpy as np
 import pytest
 
 import hierarchical_kv_cache_swap_gb300 as hs
@@ -81,3 +82,13 @@ def test_calls_on_null_context_fail_cleanly(lib):
 def test_binding_fails_loudly_without_the_library(tmp_path):
     with pytest.raises(hs.HsError):
         hs.load_library(str(tmp_path / "missing.so"))
+
+
+def test_addr_of_numpy_arrays_matches_ctypes_data():
+    """The binding's fast address path agrees with numpy's own for every kind of array."""
+    a = np.arange(64, dtype=np.int32).reshape(8, 8)
+    ro = a.copy()
+    ro.flags.writeable = False
+    cases = [a, a[3], a[2:5], a[:, 1], ro, ro[2], np.empty(0, np.int32), np.empty((0, 4), np.int32)]
+    for x in cases:
+        assert hs._addr(x) == x.ctypes.data
