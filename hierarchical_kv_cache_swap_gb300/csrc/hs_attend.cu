@@ -11,13 +11,16 @@
 // selections whose slot is valid, o_h = softmax(s_h) V, lse_h = ln sum_j exp(s_hj).
 //
 // attend_kernel: one CTA per (request b, key split s, value half v), 800 threads, one CTA
-// per SM (225 KB of shared memory, 512 TMEM columns).
-//   * Q [128 heads x 576] bf16 stays in shared memory for the whole CTA, in the 128-byte
-//     swizzled K-major layout the MMA reads (heads beyond H are zero rows).
+// per SM (209 KB of shared memory, 512 TMEM columns).
 //   * Keys come in blocks of 256 selections. 16 producer warps gather their rows through
-//     out_slots, decode the E4M3 codes times their block scale to bf16 and fill two 32 KB
-//     stages: per block nine K chunks (256 keys x 64 dims, K-major) and four V chunks
-//     (64 keys x this CTA's 256 value dims, read MN-major).
+//     out_slots, decode the E4M3 codes times their block scale to bf16 and fill a ring of
+//     four 48 KB stages: per block nine K fills (256 keys x 64 dims, K-major) and four V
+//     fills (64 keys x this CTA's 256 value dims, read MN-major).
+//   * Q [H x 576] bf16 is not kept resident: a K fill's stage also receives the matching
+//     64-dimension column of Q (128 rows x 128 bytes) by one tensor-memory-access copy
+//     (TMA, 128-byte swizzle, rows beyond H zero-filled) that lands on its own mbarrier.
+//     Freeing Q's 147 KB of shared memory is what pays for the four-deep ring, so the
+//     producers keep filling while the softmax runs.
 //   * one thread issues the MMAs: S = Q K^T (M=128 heads, N=256 keys, K=16 per
 //     instruction, 36 per block) into 256 TMEM columns, and O += P V (M=128, N=256 value
 //     dims, K=16 keys, 16 per block) with P read from TMEM; completion is signalled through
@@ -34,6 +37,7 @@
 // Every wait on an mbarrier is bounded: on expiry the CTA records HS_STATUS_TIMEOUT,
 // every role leaves its loop, the MMA thread waits (bounded) for its own MMAs, and the
 // TMEM columns are freed before the CTA exits.
+#include <cuda.h>  // CUtensorMap (the encoder is reached through the runtime's entry point)
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -50,10 +54,10 @@ constexpr int kDimV = 512;
 constexpr int kHalfV = 256;    // value dimensions per CTA
 constexpr int kBlk = 256;      // keys per block: the N of S = Q K^T
 constexpr int kChunks = kDimK / 64;                  // 64-element (128-byte) swizzle columns
-constexpr uint32_t kQChunk = kHeads * 128;           // bytes of one Q column chunk
-constexpr uint32_t kQBytes = kQChunk * kChunks;      // 147456
-constexpr uint32_t kStageBytes = 32768;              // K chunk: 256 keys x 64 dims; V chunk: 64 keys x 256 dims
-constexpr int kStages = 2;
+constexpr uint32_t kQChunk = kHeads * 128;           // bytes of one Q column chunk (16 KB)
+constexpr uint32_t kKVBytes = 32768;                 // K chunk: 256 keys x 64 dims; V chunk: 64 keys x 256 dims
+constexpr uint32_t kSlotBytes = kQChunk + kKVBytes;  // a stage: the Q chunk, then the K (or V) chunk
+constexpr int kStages = 4;
 constexpr int kKFills = kChunks;                     // K chunks per block (8 latent + 1 rotary)
 constexpr int kVKeys = 64;                           // keys per V chunk
 constexpr int kVFills = kBlk / kVKeys;               // V chunks per block
@@ -69,8 +73,11 @@ constexpr uint32_t kWaitLimit = 1u << 22;  // polls of an mbarrier before giving
 constexpr int kMaxSplitKeys = 2048;        // slots of one split staged in shared memory
 
 // barrier indices
-enum { kQFull = 0, kFull = 1, kFree = 3, kSFull = 5, kPFull = 6, kPvDone = 7, kVmFull = 8, kDrain = 10,
-       kBmax = 11 /* 2, by block parity */, kLsum = 13, kBars = 14 };
+enum { kFull = 0 /* kStages: producers' fills */, kFree = 4 /* kStages: MMAs done with a stage */,
+       kQLand = 8 /* kStages: a stage's Q chunk has landed */, kSFull = 12, kPFull = 13, kPvDone = 14,
+       kVmFull = 15 /* 2, by block parity */, kDrain = 17, kBmax = 18 /* 2, by block parity */, kLsum = 20,
+       kBars = 21 };
+static_assert(kFree == kFull + kStages && kQLand == kFree + kStages && kSFull == kQLand + kStages, "barrier map");
 
 struct Smem {  // beyond Q and the stages
     int32_t slot[kMaxSplitKeys];  // this split's out_slots
@@ -81,12 +88,11 @@ struct Smem {  // beyond Q and the stages
     uint32_t tmem;
     volatile int abort;
 };
-constexpr uint32_t kSmemBytes = 1024 + kQBytes + kStages * kStageBytes + sizeof(Smem);
+constexpr uint32_t kSmemBytes = 1024 + kStages * kSlotBytes + sizeof(Smem);
 
 struct AttendArgs {
     const uint8_t* dev;        // [R][S][656]
     int S;
-    const uint16_t* q;         // [B][H][576] bf16
     int H;
     const int32_t* out_slots;  // [B][k]
     int k;
@@ -128,6 +134,19 @@ __device__ __forceinline__ bool bar_wait(Smem* sm, uint64_t* b, uint32_t parity,
 // or none does.
 __device__ __forceinline__ bool warp_wait(Smem* sm, uint64_t* b, uint32_t parity, uint32_t* status) {
     return __all_sync(0xffffffffu, bar_wait(sm, b, parity, status));
+}
+
+// ---------------------------------------------------------------- TMA
+__device__ __forceinline__ void bar_expect_tx(uint64_t* b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+// Box (64 dims, 128 heads, 1 request) of Q at (dim x, head 0, request z) into dst (1024-byte
+// aligned), 128-byte swizzled; completion is counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_q(void* dst, const CUtensorMap* map, int x, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(su32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(0), "r"(z), "r"(su32(bar))
+        : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -217,12 +236,11 @@ __device__ __forceinline__ uint4 decode8(uint32_t lo, uint32_t hi, float scale) 
 // Byte offset of 16-byte unit u (0..7) of row r in a 128-byte-swizzled column chunk.
 __device__ __forceinline__ uint32_t swz(int r, int u) { return (uint32_t)(r * 128 + ((u ^ (r & 7)) << 4)); }
 
-__global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A) {
+__global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A, const __grid_constant__ CUtensorMap qmap) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = base;
-    uint8_t* sK = base + kQBytes;  // stage st at sK + st * kStageBytes
-    Smem* sm = reinterpret_cast<Smem*>(base + kQBytes + kStages * kStageBytes);
+    uint8_t* ring = base;  // stage st at ring + st * kSlotBytes: Q chunk, then K (or V) chunk
+    Smem* sm = reinterpret_cast<Smem*>(base + kStages * kSlotBytes);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int v = blockIdx.x & 1;
     const int split = (blockIdx.x >> 1) % A.nsplit;
@@ -232,12 +250,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
     const int nb = kend > kbeg ? (kend - kbeg + kBlk - 1) / kBlk : 0;
 
     if (tid == 0) {
-        bar_init(&sm->bar[kQFull], kProdWarps * 32);
         for (int st = 0; st < kStages; ++st) {
             bar_init(&sm->bar[kFull + st], kProdWarps * 32);
             bar_init(&sm->bar[kFree + st], 1);
-            bar_init(&sm->bar[kVmFull + st], kBlk / 32);
+            bar_init(&sm->bar[kQLand + st], 1);
         }
+        bar_init(&sm->bar[kVmFull], kBlk / 32);
+        bar_init(&sm->bar[kVmFull + 1], kBlk / 32);
         bar_init(&sm->bar[kSFull], 1);
         bar_init(&sm->bar[kPFull], kSoftWarps * 32);
         bar_init(&sm->bar[kPvDone], 1);
@@ -262,17 +281,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
         // ------------------------------------------------------------ producers
         const int pw = warp - kSoftWarps;
         const int ptid = tid - kSoftWarps * 32;  // 0..255
-        {  // Q, once, by asynchronous copies (rows h >= H are zero-filled)
-            const uint8_t* qb = reinterpret_cast<const uint8_t*>(A.q + (size_t)b * A.H * kDimK);
-            for (int u = ptid; u < kHeads * (kDimK / 8); u += kProdWarps * 32) {
-                const int h = u / (kDimK / 8), cu = u - h * (kDimK / 8);
-                const uint32_t dst = su32(sQ + (cu >> 3) * kQChunk + swz(h, cu & 7));
-                const uint8_t* src = qb + ((size_t)min(h, A.H - 1) * (kDimK / 8) + cu) * 16;
-                const uint32_t n = h < A.H ? 16u : 0u;
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
-            }
-            asm volatile("cp.async.commit_group;" ::: "memory");
-        }
         // the split's slots, staged once
         const int32_t* slots = A.out_slots + (size_t)b * A.k;
         for (int j = ptid; j < kend - kbeg; j += kProdWarps * 32) sm->slot[j] = __ldg(slots + kbeg + j);
@@ -288,9 +296,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
             if (s >= 0) asm volatile("cp.async.bulk.prefetch.L2.global [%0], 656;" ::"l"(row_of(s)) : "memory");
         };
         prefetch_block(0);
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        bar_arrive(&sm->bar[kQFull]);
         // Stage fills, in the order the MMAs consume them: per block the 9 K chunks (8
         // latent, then the rotary one) and the 4 V chunks. Loads are spread so that the
         // lanes of a warp read a few whole stretches of a row each (4 lanes x 16 bytes
@@ -304,26 +309,40 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
             float scale[kW];
         };
         const int total = nb * kFills;
+        uint32_t qpar = 0, qout = 0;  // (thread 0) per stage: phase parity of its next Q copy; copies issued
         const int kq = ptid & 3, kkey = ptid >> 2;    // K chunk: quarter of the 64 dims, key (+128 w)
         const int vu = ptid & 15, vkey = ptid >> 4;   // V chunk: 16-dim unit of the half, key (+32 w)
         const int rq = ptid & 7, rkey = ptid >> 3;    // rotary chunk: 16-byte unit, key (+64 w)
+        // This thread's K rows are the same for the eight latent fills of a block: they are
+        // looked up once per block (a shared-memory read before every load would queue
+        // behind the stage stores and delay the loads' issue).
+        const uint8_t* krow[kW];
+        int kblock = -1;
         auto issue = [&](int g, Raw& r) {
             if (g >= total) return;
             const int i = g / kFills, f = g - i * kFills;
             if (f == kKFills - 1) return;  // the rotary chunk is copied asynchronously
+            if (f < kKFills && i != kblock) {
+#pragma unroll
+                for (int w = 0; w < kW; ++w) {
+                    const int32_t s = slot_at(i * kBlk + kkey + 128 * w);
+                    krow[w] = s >= 0 ? row_of(s) : nullptr;
+                }
+                kblock = i;
+            }
 #pragma unroll
             for (int w = 0; w < kW; ++w) {
-                int32_t s;
+                const uint8_t* row;
                 int off;
                 if (f < kKFills) {
-                    s = slot_at(i * kBlk + kkey + 128 * w);
+                    row = krow[w];
                     off = 64 * f + 16 * kq;
                 } else {
-                    s = slot_at(i * kBlk + (f - kKFills) * kVKeys + vkey + 32 * w);
+                    const int32_t s = slot_at(i * kBlk + (f - kKFills) * kVKeys + vkey + 32 * w);
+                    row = s >= 0 ? row_of(s) : nullptr;
                     off = kHalfV * v + 16 * vu;
                 }
-                if (s >= 0) {
-                    const uint8_t* row = row_of(s);
+                if (row) {
                     r.c[w] = __ldg(reinterpret_cast<const uint4*>(row + off));
                     r.scale[w] = __ldg(reinterpret_cast<const float*>(row + 512) + (off >> 7));
                 } else {
@@ -342,9 +361,16 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
                 }
             }
             if (pw < kBlk / 32 && f == pw) prefetch_block(i + 1);  // the next block's rows into L2
-            const int st = g & 1;
-            if (g >= 2 && !bar_wait(sm, &sm->bar[kFree + st], ((g >> 1) & 1) ^ 1, A.status)) return false;
-            uint8_t* stg = sK + st * kStageBytes;
+            const int st = g % kStages;
+            if (g >= kStages && !bar_wait(sm, &sm->bar[kFree + st], ((g / kStages) & 1) ^ 1, A.status)) return false;
+            uint8_t* slot = ring + st * kSlotBytes;
+            if (f < kKFills && ptid == 0) {  // the matching 64-dimension column of Q, by one TMA copy
+                bar_expect_tx(&sm->bar[kQLand + st], kQChunk);
+                tma_load_q(slot, &qmap, 64 * f, b, &sm->bar[kQLand + st]);
+                qpar ^= 1u << st;
+                qout |= 1u << st;
+            }
+            uint8_t* stg = slot + kQChunk;
             if (f == kKFills - 1) {  // rotary values: bf16 already, copied as they are
 #pragma unroll
                 for (int w = 0; w < 2 * kW; ++w) {
@@ -387,26 +413,38 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
             issue(g + 4, r1);
             if (!process(g + 2, r2)) break;
         }
+        // No Q copy may still be landing when the CTA exits (after an abort the MMA thread
+        // may not have waited for the last ones): wait, bounded, for the last copy issued
+        // into each stage.
+        if (ptid == 0)
+            for (int st = 0; st < kStages; ++st)
+                if ((qout >> st) & 1u) {
+                    const uint32_t par = ((qpar >> st) & 1u) ^ 1u;
+                    for (uint32_t it = 0; it < kWaitLimit && !bar_try(&sm->bar[kQLand + st], par); ++it) {
+                    }
+                }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issue (one thread)
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16(kHeads, kBlk, 0);
             const uint32_t id_o = idesc_bf16(kHeads, kHalfV, 1);
-            const uint32_t q0 = su32(sQ), k0 = su32(sK);
-            bool ok = bar_wait(sm, &sm->bar[kQFull], 0, A.status);
-            uint32_t g = 0;
+            const uint32_t s0 = su32(ring);
+            bool ok = true;
+            uint32_t g = 0, qpar = 0;  // qpar: per stage, phase parity of the next Q copy to wait for
             for (int i = 0; ok && i < nb; ++i) {
                 // S and P share columns: block i's scores wait until block i-1's product is done
                 if (i > 0 && !bar_wait(sm, &sm->bar[kPvDone], (i - 1) & 1, A.status)) { ok = false; break; }
                 for (int c = 0; c < kKFills; ++c, ++g) {
-                    const int st = g & 1;
-                    if (!bar_wait(sm, &sm->bar[kFull + st], (g >> 1) & 1, A.status)) { ok = false; break; }
+                    const int st = g % kStages;
+                    if (!bar_wait(sm, &sm->bar[kFull + st], (g / kStages) & 1, A.status) ||
+                        !bar_wait(sm, &sm->bar[kQLand + st], (qpar >> st) & 1u, A.status)) { ok = false; break; }
+                    qpar ^= 1u << st;
                     fence_after();
-                    const uint32_t kb = k0 + st * kStageBytes;
+                    const uint32_t qa = s0 + st * kSlotBytes, kb = qa + kQChunk;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_ss(tmem + kColS, smem_desc(q0 + c * kQChunk + kk * 32, 16, 1024),
-                               smem_desc(kb + kk * 32, 16, 1024), id_s, (c | kk) ? 1u : 0u);
+                        mma_ss(tmem + kColS, smem_desc(qa + kk * 32, 16, 1024), smem_desc(kb + kk * 32, 16, 1024),
+                               id_s, (c | kk) ? 1u : 0u);
                     mma_commit(&sm->bar[kFree + st]);
                 }
                 if (!ok) break;
@@ -414,10 +452,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A)
                 if (!bar_wait(sm, &sm->bar[kPFull], i & 1, A.status)) { ok = false; break; }
                 fence_after();
                 for (int vc = 0; vc < kVFills; ++vc, ++g) {
-                    const int st = g & 1;
-                    if (!bar_wait(sm, &sm->bar[kFull + st], (g >> 1) & 1, A.status)) { ok = false; break; }
+                    const int st = g % kStages;
+                    if (!bar_wait(sm, &sm->bar[kFull + st], (g / kStages) & 1, A.status)) { ok = false; break; }
                     fence_after();
-                    const uint32_t vb = k0 + st * kStageBytes;
+                    const uint32_t vb = s0 + st * kSlotBytes + kQChunk;
 #pragma unroll
                     for (int ks = 0; ks < kVKeys / 16; ++ks)
                         mma_ts(tmem + kColO, tmem + kColS + (kVKeys / 2) * vc + 8 * ks + (vc >= kVFills / 2 ? 64 : 0),
@@ -583,6 +621,42 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
     if (threadIdx.x == 0) lse[(size_t)b * H + h] = mx > -INFINITY ? mx + logf(L) : -INFINITY;
 }
 
+// The driver's tensor-map encoder, looked up once through the runtime (no link against
+// the driver library).
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiled encoder() {
+    static const EncodeTiled fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult found;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &found) !=
+                cudaSuccess ||
+            found != cudaDriverEntryPointSuccess) {
+            (void)cudaGetLastError();
+            return (EncodeTiled) nullptr;
+        }
+        return reinterpret_cast<EncodeTiled>(f);
+    }();
+    return fn;
+}
+
+// Q [B][H][576] bf16 as a 3-D tensor (dims, heads, requests); one box is a 64-dimension
+// column of all 128 head rows of one request (rows >= H read as zero), 128-byte swizzled
+// as the MMA's K-major operand.
+cudaError_t encode_q_map(CUtensorMap* map, const uint16_t* q, int B, int H) {
+    const EncodeTiled enc = encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)kDimK, (cuuint64_t)H, (cuuint64_t)B};
+    const cuuint64_t strides[2] = {(cuuint64_t)kDimK * 2, (cuuint64_t)H * kDimK * 2};  // bytes, dims 1 and 2
+    const cuuint32_t box[3] = {64, (cuuint32_t)kHeads, 1};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(q), dims, strides, box,
+                           estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 size_t attend_smem_bytes() { return kSmemBytes; }
@@ -613,10 +687,12 @@ cudaError_t configure_attend() {
 cudaError_t launch_attend(const Layout& L, cudaStream_t stream, const uint16_t* q, int B, int H,
                           const int32_t* out_slots, int k, float sm_scale, float* o, float* lse,
                           void* workspace, const AttendPlan& plan) {
+    CUtensorMap qmap;
+    cudaError_t e = encode_q_map(&qmap, q, B, H);
+    if (e != cudaSuccess) return e;
     AttendArgs a;
     a.dev = L.dev;
     a.S = L.S;
-    a.q = q;
     a.H = H;
     a.out_slots = out_slots;
     a.k = k;
@@ -635,8 +711,8 @@ cudaError_t launch_attend(const Layout& L, cudaStream_t stream, const uint16_t* 
         a.o = o;
         a.lse = lse;
     }
-    attend_kernel<<<B * plan.nsplit * 2, kThreads, kSmemBytes, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
+    attend_kernel<<<B * plan.nsplit * 2, kThreads, kSmemBytes, stream>>>(a, qmap);
+    e = cudaGetLastError();
     if (e != cudaSuccess || plan.nsplit == 1) return e;
     combine_kernel<<<B * H, 128, 0, stream>>>(part_o, part_lse, plan.nsplit, H, o, lse);
     return cudaGetLastError();
