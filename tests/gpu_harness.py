@@ -16,7 +16,7 @@ import tracegen
 from oracle import Oracle
 
 
-class GpuRun:
+class DeviceRun:
     """A context plus the whole trace resident on the device."""
 
     def __init__(self, w: tracegen.Workload, T: int, B: int | None = None, layer: int = 0,
@@ -50,7 +50,7 @@ class GpuRun:
 
 
 def run_and_compare(w: tracegen.Workload, T: int, B: int | None = None, sample=None,
-                    checkpoints=None, layer: int = 0, run: GpuRun | None = None,
+                    checkpoints=None, layer: int = 0, run: DeviceRun | None = None,
                     policy: int = 0, seed: int = 0) -> dict:
     """Run T steps on the GPU, then replay the sampled requests on the oracle, both
     under replacement `policy` (0 LRU, 1 FIFO, 2 RANDOM with `seed`).
@@ -59,7 +59,7 @@ def run_and_compare(w: tracegen.Workload, T: int, B: int | None = None, sample=N
     the first difference.
     """
     own = run is None
-    run = run or GpuRun(w, T, B, layer=layer)
+    run = run or DeviceRun(w, T, B, layer=layer)
     B = run.B
     sample = list(range(B)) if sample is None else list(sample)
     checkpoints = sorted(set(checkpoints or [T - 1]))

@@ -13,7 +13,7 @@ import torch
 import hierarchical_kv_cache_swap_gb300 as hs
 import tracegen
 from oracle import Oracle
-from tests.gpu_harness import GpuRun, run_and_compare
+from tests.gpu_harness import DeviceRun, run_and_compare
 
 pytestmark = pytest.mark.gpu
 
@@ -60,7 +60,7 @@ def test_quest_pages_eight_layers_reduced_batch():
     B, T = 8, 48
     sel = tracegen.trace(w, T=T, B=B)
     for layer in range(w.L):
-        run = GpuRun(w, T, B=B, layer=layer, sel=sel)
+        run = DeviceRun(w, T, B=B, layer=layer, sel=sel)
         run_and_compare(w, T=T, B=B, checkpoints=[0, 7, T - 1], layer=layer, run=run)
         run.close()
 
@@ -92,7 +92,7 @@ def test_policy_switch_mid_trace():
     """The state carries over when the policy changes between calls."""
     w = tracegen.WORKLOADS["tiny"]
     T = 30
-    run = GpuRun(w, T)
+    run = DeviceRun(w, T)
     o = Oracle(run.B, w.C, w.S, w.E)
     host = run.ctx.host_kv()
     for t in range(T):
@@ -116,7 +116,7 @@ def test_policy_switch_mid_trace():
 
 def test_noio_all_hits_after_first_call():
     w = tracegen.noio_workload(4096)
-    run = GpuRun(w, T=12, fill=False)
+    run = DeviceRun(w, T=12, fill=False)
     for t in range(12):
         run.step(t)
     miss = run.miss_dev.cpu().numpy()
@@ -200,8 +200,8 @@ def test_padding_out_of_range_and_duplicates_set_status():
 
 def test_permutation_invariance():
     w = tracegen.WORKLOADS["tiny"]
-    a = GpuRun(w, T=20)
-    b = GpuRun(w, T=20)
+    a = DeviceRun(w, T=20)
+    b = DeviceRun(w, T=20)
     rng = np.random.default_rng(1)
     perms = [rng.permutation(w.k) for _ in range(20)]
     b.sel_dev = torch.from_numpy(np.stack([a.sel[t][:, perms[t]] for t in range(20)])).cuda()
@@ -221,8 +221,8 @@ def test_graph_replay_equals_eager():
     """The step can be captured in a CUDA graph; replays advance the state like eager calls."""
     w = tracegen.WORKLOADS["dsa"]
     T = 24
-    eager = GpuRun(w, T, B=8)
-    graph = GpuRun(w, T, B=8)
+    eager = DeviceRun(w, T, B=8)
+    graph = DeviceRun(w, T, B=8)
     for t in range(T):
         eager.step(t)
     s = torch.cuda.Stream()
@@ -259,7 +259,7 @@ def _host_buffer(shape, pinned):
 def test_host_buffer_entry_point_matches_device_entry_point(sel_pinned, out_pinned):
     w = tracegen.WORKLOADS["dsa"]
     T = 10
-    a = GpuRun(w, T, B=4)
+    a = DeviceRun(w, T, B=4)
     b = hs.Context(4, w.C, w.S, w.E)
     tracegen.fill_kv(b.host_kv_address(), b.host_stride, w, B=4)
     sel = _host_buffer(a.sel.shape, sel_pinned)
@@ -280,8 +280,8 @@ def test_host_buffer_entry_point_matches_device_entry_point(sel_pinned, out_pinn
 
 def test_no_copy_flag_keeps_bookkeeping_and_skips_fetch():
     w = tracegen.WORKLOADS["tiny"]
-    a = GpuRun(w, T=16)
-    b = GpuRun(w, T=16)
+    a = DeviceRun(w, T=16)
+    b = DeviceRun(w, T=16)
     b.ctx.set_flags(hs.HS_FLAG_NO_COPY)
     assert a.ctx.kernels_per_call() == 2 and b.ctx.kernels_per_call() == 1
     for t in range(16):
@@ -297,7 +297,7 @@ def test_no_copy_flag_keeps_bookkeeping_and_skips_fetch():
 
 def test_reset_restores_empty_state():
     w = tracegen.WORKLOADS["tiny"]
-    run = GpuRun(w, T=8)
+    run = DeviceRun(w, T=8)
     for t in range(8):
         run.step(t)
     run.ctx.reset()
@@ -327,8 +327,8 @@ def test_contexts_of_different_sizes_coexist():
     big = tracegen.WORKLOADS["dsa"]
     small = tracegen.Workload("small", 9, B=2, L=1, C=64, S=16, k=8, E=16, kv_kind=tracegen.KV_RAW,
                               T=6, keep_pct=50, zipf_s=1.1, seed=3)
-    a = GpuRun(big, T=6, B=2)
-    b = GpuRun(small, T=6)
+    a = DeviceRun(big, T=6, B=2)
+    b = DeviceRun(small, T=6)
     for t in range(6):
         a.step(t)
         b.step(t)
@@ -345,7 +345,7 @@ def test_no_copy_calls_interleaved_with_fetching_calls():
     fetching calls must still match the oracle."""
     w = tracegen.WORKLOADS["dsa"]
     B, T = 4, 24
-    run = GpuRun(w, T, B=B)
+    run = DeviceRun(w, T, B=B)
     o = Oracle(B, w.C, w.S, w.E)
     base = run.ctx.host_kv_address()
     row_bytes = w.C * run.ctx.host_stride
