@@ -92,3 +92,22 @@ def test_addr_of_numpy_arrays_matches_ctypes_data():
     cases = [a, a[3], a[2:5], a[:, 1], ro, ro[2], np.empty(0, np.int32), np.empty((0, 4), np.int32)]
     for x in cases:
         assert hs._addr(x) == x.ctypes.data
+
+
+def test_resolve_host_rejects_bad_buffers_before_any_call():
+    """The host-buffer entry point's binding checks dtype, layout and shapes before it
+    reaches the library (so no context, and no GPU, is needed to exercise them)."""
+    ctx = object.__new__(hs.Context)
+    sel = np.zeros((2, 4), np.int32)
+    out = np.zeros((2, 4), np.int32)
+    miss = np.zeros(2, np.int32)
+    bad = [
+        (sel.astype(np.int64), out, miss),            # wrong dtype
+        (sel, np.zeros((2, 8), np.int32)[:, ::2], miss),  # not contiguous
+        (sel, np.zeros((2, 3), np.int32), miss),      # out_slots shape
+        (sel, out, np.zeros(3, np.int32)),            # miss_counts shape
+        (sel.tolist(), out, miss),                    # not an array
+    ]
+    for args in bad:
+        with pytest.raises(ValueError):
+            ctx.resolve_host(*args)
