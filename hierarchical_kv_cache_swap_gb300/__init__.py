@@ -28,6 +28,7 @@ HS_STATUS_DUP = 2
 HS_STATUS_STEP_LIMIT = 4
 HS_STATUS_TIMEOUT = 8
 HS_FLAG_NO_COPY = 1
+HS_FLAG_TEST_STALL = 2
 POLICY_LRU, POLICY_FIFO, POLICY_RANDOM = 0, 1, 2
 
 # every symbol include/hs.h declares, with (restype, argtypes)
@@ -69,6 +70,7 @@ SIGNATURES = {
     "hs_clear_status": (_I, [_VP]),
     "hs_set_flags": (_I, [_VP, _U]),
     "hs_set_policy": (_I, [_VP, _I, ctypes.c_uint64]),
+    "hs_set_wait_limit": (_I, [_VP, ctypes.c_uint64]),
     "hs_attend": (_I, [_VP, _VP, _VP, _I, _I, _VP, _I, ctypes.c_float, _VP, _VP, _VP, ctypes.c_size_t]),
     "hs_attend_workspace": (_I, [_VP, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
     "hs_kernels_per_call": (_I, [_VP]),
@@ -318,6 +320,10 @@ class Context:
     def set_policy(self, policy: int, seed: int = 0) -> None:
         """Replacement policy (POLICY_LRU / POLICY_FIFO / POLICY_RANDOM) of later calls."""
         self._check(self._lib.hs_set_policy(self._h, policy, seed & (2**64 - 1)), "hs_set_policy")
+
+    def set_wait_limit(self, ns: int) -> None:
+        """Time limit (global-timer ns from a CTA's start) of the kernels' device waits."""
+        self._check(self._lib.hs_set_wait_limit(self._h, int(ns)), "hs_set_wait_limit")
 
     def kernels_per_call(self) -> int:
         return int(self._lib.hs_kernels_per_call(self._h))

@@ -102,14 +102,18 @@ int check_call(hs_ctx* h, const void* sel, int B, int k, const void* out, const 
 
 int enqueue(hs_ctx* h, cudaStream_t s, const int32_t* sel, int k, int32_t* out, int32_t* miss,
             cudaEvent_t* ev) {
-    const bool fetch = !(h->flags & HS_FLAG_NO_COPY);
+    bool fetch = !(h->flags & HS_FLAG_NO_COPY);
+    // chained by programmatic dependent launch unless events sit between the kernels
+    const bool pdl = ev == nullptr && hs::overlap_fetch(h->L.R, h->num_sms);
+    // A stalled resolution publishes nothing. Only a fetch grid that waits for the flags
+    // (the overlapped one) may follow it: the others would read a stale hand-off.
+    h->L.no_publish = (h->flags & HS_FLAG_TEST_STALL) ? 1 : 0;
+    if (h->L.no_publish && !pdl) fetch = false;
     cudaError_t e;
     if (ev && (e = cudaEventRecord(ev[0], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     if ((e = hs::launch_resolve(h->L, s, sel, k, out, miss, fetch)) != cudaSuccess)
         return cuda_fail(e, "resolution kernel launch");
     if (ev && (e = cudaEventRecord(ev[1], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    // chained by programmatic dependent launch unless events sit between the kernels
-    const bool pdl = ev == nullptr && hs::overlap_fetch(h->L.R, h->num_sms);
     if (fetch && (e = hs::launch_gather(h->L, s, out, k, h->num_sms, pdl)) != cudaSuccess)
         return cuda_fail(e, "fetch kernel launch");
     if (ev && (e = cudaEventRecord(ev[2], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
@@ -378,7 +382,7 @@ int hs_attend(hs_ctx* h, hs_stream_t stream, const void* q, int B, int H, const 
         return fail(HS_ERR_INVALID, "workspace of %zu bytes (16-byte aligned) needed, %zu given", plan.workspace_bytes,
                     workspace_bytes);
     cudaError_t e = hs::launch_attend(h->L, (cudaStream_t)stream, (const uint16_t*)q, B, H, out_slots, k, sm_scale, o,
-                                      lse, workspace, plan);
+                                      lse, workspace, plan, (h->flags & HS_FLAG_TEST_STALL) != 0);
     if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
     g_err[0] = 0;
     return HS_OK;
@@ -491,8 +495,18 @@ int hs_clear_status(hs_ctx* h) {
 
 int hs_set_flags(hs_ctx* h, unsigned flags) {
     if (!h) return fail(HS_ERR_INVALID, "null context");
-    if (flags & ~(unsigned)HS_FLAG_NO_COPY) return fail(HS_ERR_INVALID, "unknown flags 0x%x", flags);
+    if (flags & ~(unsigned)(HS_FLAG_NO_COPY | HS_FLAG_TEST_STALL))
+        return fail(HS_ERR_INVALID, "unknown flags 0x%x", flags);
     h->flags = flags;
+    return HS_OK;
+}
+
+int hs_set_wait_limit(hs_ctx* h, uint64_t ns) {
+    if (!h) return fail(HS_ERR_INVALID, "null context");
+    if (ns < hs::kMinWaitNs || ns > hs::kMaxWaitNs)
+        return fail(HS_ERR_INVALID, "wait limit %llu ns outside [%llu, %llu]", (unsigned long long)ns,
+                    (unsigned long long)hs::kMinWaitNs, (unsigned long long)hs::kMaxWaitNs);
+    h->L.wait_ns = ns;
     return HS_OK;
 }
 
@@ -507,7 +521,9 @@ int hs_set_policy(hs_ctx* h, int policy, uint64_t seed) {
 
 int hs_kernels_per_call(hs_ctx* h) {
     if (!h) return fail(HS_ERR_INVALID, "null context");
-    return (h->flags & HS_FLAG_NO_COPY) ? 1 : 2;
+    if (h->flags & HS_FLAG_NO_COPY) return 1;
+    if ((h->flags & HS_FLAG_TEST_STALL) && !hs::overlap_fetch(h->L.R, h->num_sms)) return 1;
+    return 2;
 }
 
 }  // extern "C"

@@ -34,9 +34,10 @@
 // With several key splits per request each CTA writes its normalised partial and its
 // lse; combine_kernel merges them (weights exp(lse_s - lse)).
 //
-// Every wait on an mbarrier is bounded: on expiry the CTA records HS_STATUS_TIMEOUT,
-// every role leaves its loop, the MMA thread waits (bounded) for its own MMAs, and the
-// TMEM columns are freed before the CTA exits.
+// Every wait on an mbarrier is bounded in time (global timer, the context's wait limit
+// counted from the CTA's start): on expiry the CTA records HS_STATUS_TIMEOUT, every role
+// leaves its loop, the MMA thread waits (again bounded in time) for its own MMAs and the
+// producers for their last Q copies, and the TMEM columns are freed before the CTA exits.
 #include <cuda.h>  // CUtensorMap (the encoder is reached through the runtime's entry point)
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -69,7 +70,6 @@ constexpr int kMmaWarp = kSoftWarps + kProdWarps;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256;  // O: 256 columns; S: 256 columns, P (bf16) written over its first 128
 constexpr float kRescaleLog2 = 8.0f;
-constexpr uint32_t kWaitLimit = 1u << 22;  // polls of an mbarrier before giving up
 constexpr int kMaxSplitKeys = 2048;        // slots of one split staged in shared memory
 
 // barrier indices
@@ -101,6 +101,8 @@ struct AttendArgs {
     float* o;                  // nsplit == 1: [B][H][512]; else partials [B][nsplit][H][512]
     float* lse;                // nsplit == 1: [B][H];      else partials [B][nsplit][H]
     uint32_t* status;
+    uint64_t wait_ns;          // time limit of the CTA's waits (global-timer ns from its start)
+    int stall;                 // tests: the producers withhold the first fill
 };
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -118,22 +120,32 @@ __device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t parity) {
                  : "=r"(ok) : "r"(su32(b)), "r"(parity) : "memory");
     return ok != 0;
 }
-// Waits for the phase of `parity` to complete; false (and the CTA aborted) on expiry or
-// when another role has aborted.
-__device__ __forceinline__ bool bar_wait(Smem* sm, uint64_t* b, uint32_t parity, uint32_t* status) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i) {
-        if (bar_try(b, parity)) return true;
+// Waits for the phase of `parity` to complete; false (and the CTA aborted) once the
+// global timer passes `deadline` or when another role has aborted.
+__device__ __forceinline__ bool bar_wait(Smem* sm, uint64_t* b, uint32_t parity, uint32_t* status, uint64_t deadline) {
+    while (!bar_try(b, parity)) {
         if (sm->abort) return false;
+        if (global_ns() > deadline) {
+            sm->abort = 1;
+            atomicOr(status, 8u /* HS_STATUS_TIMEOUT */);
+            return false;
+        }
     }
-    sm->abort = 1;
-    atomicOr(status, 8u /* HS_STATUS_TIMEOUT */);
-    return false;
+    return true;
 }
 
 // The same wait taken by a whole warp whose next step is warp-collective: all lanes go on
 // or none does.
-__device__ __forceinline__ bool warp_wait(Smem* sm, uint64_t* b, uint32_t parity, uint32_t* status) {
-    return __all_sync(0xffffffffu, bar_wait(sm, b, parity, status));
+__device__ __forceinline__ bool warp_wait(Smem* sm, uint64_t* b, uint32_t parity, uint32_t* status, uint64_t deadline) {
+    return __all_sync(0xffffffffu, bar_wait(sm, b, parity, status, deadline));
+}
+
+// Waits (bounded by `deadline` only, whatever the abort flag says) for in-flight
+// asynchronous work -- a TMA copy or the CTA's MMAs -- that must land before the CTA
+// releases its shared memory or tensor memory.
+__device__ __forceinline__ void drain_wait(uint64_t* b, uint32_t parity, uint64_t deadline) {
+    while (!bar_try(b, parity) && global_ns() <= deadline) {
+    }
 }
 
 // ---------------------------------------------------------------- TMA
@@ -248,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
     const int kbeg = split * A.keys_per_split;
     const int kend = min(A.k, kbeg + A.keys_per_split);
     const int nb = kend > kbeg ? (kend - kbeg + kBlk - 1) / kBlk : 0;
+    const uint64_t deadline = global_ns() + A.wait_ns;  // every wait of this CTA ends by then
 
     if (tid == 0) {
         for (int st = 0; st < kStages; ++st) {
@@ -362,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
             }
             if (pw < kBlk / 32 && f == pw) prefetch_block(i + 1);  // the next block's rows into L2
             const int st = g % kStages;
-            if (g >= kStages && !bar_wait(sm, &sm->bar[kFree + st], ((g / kStages) & 1) ^ 1, A.status)) return false;
+            if (g >= kStages && !bar_wait(sm, &sm->bar[kFree + st], ((g / kStages) & 1) ^ 1, A.status, deadline)) return false;
             uint8_t* slot = ring + st * kSlotBytes;
             if (f < kKFills && ptid == 0) {  // the matching 64-dimension column of Q, by one TMA copy
                 bar_expect_tx(&sm->bar[kQLand + st], kQChunk);
@@ -399,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
                 }
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            bar_arrive(&sm->bar[kFull + st]);
+            if (!(A.stall && g == 0)) bar_arrive(&sm->bar[kFull + st]);
             return true;
         };
         Raw r0, r1, r2;
@@ -416,13 +429,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
         // No Q copy may still be landing when the CTA exits (after an abort the MMA thread
         // may not have waited for the last ones): wait, bounded, for the last copy issued
         // into each stage.
-        if (ptid == 0)
+        if (ptid == 0) {
+            const uint64_t drain_by = global_ns() + A.wait_ns;
             for (int st = 0; st < kStages; ++st)
-                if ((qout >> st) & 1u) {
-                    const uint32_t par = ((qpar >> st) & 1u) ^ 1u;
-                    for (uint32_t it = 0; it < kWaitLimit && !bar_try(&sm->bar[kQLand + st], par); ++it) {
-                    }
-                }
+                if ((qout >> st) & 1u) drain_wait(&sm->bar[kQLand + st], ((qpar >> st) & 1u) ^ 1u, drain_by);
+        }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issue (one thread)
         if (lane == 0) {
@@ -433,11 +444,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
             uint32_t g = 0, qpar = 0;  // qpar: per stage, phase parity of the next Q copy to wait for
             for (int i = 0; ok && i < nb; ++i) {
                 // S and P share columns: block i's scores wait until block i-1's product is done
-                if (i > 0 && !bar_wait(sm, &sm->bar[kPvDone], (i - 1) & 1, A.status)) { ok = false; break; }
+                if (i > 0 && !bar_wait(sm, &sm->bar[kPvDone], (i - 1) & 1, A.status, deadline)) { ok = false; break; }
                 for (int c = 0; c < kKFills; ++c, ++g) {
                     const int st = g % kStages;
-                    if (!bar_wait(sm, &sm->bar[kFull + st], (g / kStages) & 1, A.status) ||
-                        !bar_wait(sm, &sm->bar[kQLand + st], (qpar >> st) & 1u, A.status)) { ok = false; break; }
+                    if (!bar_wait(sm, &sm->bar[kFull + st], (g / kStages) & 1, A.status, deadline) ||
+                        !bar_wait(sm, &sm->bar[kQLand + st], (qpar >> st) & 1u, A.status, deadline)) { ok = false; break; }
                     qpar ^= 1u << st;
                     fence_after();
                     const uint32_t qa = s0 + st * kSlotBytes, kb = qa + kQChunk;
@@ -449,11 +460,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
                 }
                 if (!ok) break;
                 mma_commit(&sm->bar[kSFull]);
-                if (!bar_wait(sm, &sm->bar[kPFull], i & 1, A.status)) { ok = false; break; }
+                if (!bar_wait(sm, &sm->bar[kPFull], i & 1, A.status, deadline)) { ok = false; break; }
                 fence_after();
                 for (int vc = 0; vc < kVFills; ++vc, ++g) {
                     const int st = g % kStages;
-                    if (!bar_wait(sm, &sm->bar[kFull + st], (g / kStages) & 1, A.status)) { ok = false; break; }
+                    if (!bar_wait(sm, &sm->bar[kFull + st], (g / kStages) & 1, A.status, deadline)) { ok = false; break; }
                     fence_after();
                     const uint32_t vb = s0 + st * kSlotBytes + kQChunk;
 #pragma unroll
@@ -467,8 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
             }
             // whatever happened, every MMA issued here completes before the columns are freed
             mma_commit(&sm->bar[kDrain]);
-            for (uint32_t it = 0; it < kWaitLimit && !bar_try(&sm->bar[kDrain], 0); ++it) {
-            }
+            drain_wait(&sm->bar[kDrain], 0, global_ns() + A.wait_ns);
         }
         __syncwarp();
     } else {
@@ -484,8 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int i = 0; i < nb; ++i) {
-            if (!warp_wait(sm, &sm->bar[kSFull], i & 1, A.status) ||
-                !warp_wait(sm, &sm->bar[kVmFull + (i & 1)], (i >> 1) & 1, A.status)) { ok = false; break; }
+            if (!warp_wait(sm, &sm->bar[kSFull], i & 1, A.status, deadline) ||
+                !warp_wait(sm, &sm->bar[kVmFull + (i & 1)], (i >> 1) & 1, A.status, deadline)) { ok = false; break; }
             fence_after();
             // pass 1: this group's part of the block maximum, then the block's
             float mb = -INFINITY;
@@ -501,14 +511,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
             }
             sm->bmax[i & 1][grp][h] = mb;
             bar_arrive(&sm->bar[kBmax + (i & 1)]);
-            if (!warp_wait(sm, &sm->bar[kBmax + (i & 1)], (i >> 1) & 1, A.status)) { ok = false; break; }
+            if (!warp_wait(sm, &sm->bar[kBmax + (i & 1)], (i >> 1) & 1, A.status, deadline)) { ok = false; break; }
             mb = fmaxf(sm->bmax[i & 1][0][h], sm->bmax[i & 1][1][h]);
             const bool need = mb > m + kRescaleLog2 || (m == -INFINITY && mb > -INFINITY);
             const float m_new = need ? mb : m;
             if (i > 0 && __any_sync(0xffffffffu, need)) {
                 // O holds blocks 0..i-1 (their product is done: the scores of block i
                 // were computed after it): each group rescales half of its columns to m_new
-                if (!warp_wait(sm, &sm->bar[kPvDone], (i - 1) & 1, A.status)) { ok = false; break; }
+                if (!warp_wait(sm, &sm->bar[kPvDone], (i - 1) & 1, A.status, deadline)) { ok = false; break; }
                 fence_after();
                 const float f = need ? ex2(m - m_new) : 1.f;  // m = -inf: O is zero so far
 #pragma unroll 1
@@ -550,9 +560,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
         // the running sum is the two groups' parts
         sm->lsum[grp][h] = l;
         bar_arrive(&sm->bar[kLsum]);
-        if (ok && !warp_wait(sm, &sm->bar[kLsum], 0, A.status)) ok = false;
+        if (ok && !warp_wait(sm, &sm->bar[kLsum], 0, A.status, deadline)) ok = false;
         l = sm->lsum[0][h] + sm->lsum[1][h];
-        if (ok && nb > 0 && warp_wait(sm, &sm->bar[kPvDone], (nb - 1) & 1, A.status)) {
+        if (ok && nb > 0 && warp_wait(sm, &sm->bar[kPvDone], (nb - 1) & 1, A.status, deadline)) {
             fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             size_t orow;
@@ -686,7 +696,7 @@ cudaError_t configure_attend() {
 
 cudaError_t launch_attend(const Layout& L, cudaStream_t stream, const uint16_t* q, int B, int H,
                           const int32_t* out_slots, int k, float sm_scale, float* o, float* lse,
-                          void* workspace, const AttendPlan& plan) {
+                          void* workspace, const AttendPlan& plan, bool stall) {
     CUtensorMap qmap;
     cudaError_t e = encode_q_map(&qmap, q, B, H);
     if (e != cudaSuccess) return e;
@@ -700,6 +710,8 @@ cudaError_t launch_attend(const Layout& L, cudaStream_t stream, const uint16_t* 
     a.keys_per_split = plan.keys_per_split;
     a.scale_log2 = sm_scale * 1.4426950408889634f;
     a.status = L.status;
+    a.wait_ns = L.wait_ns;
+    a.stall = stall ? 1 : 0;
     float* part_o = nullptr;
     float* part_lse = nullptr;
     if (plan.nsplit > 1) {

@@ -20,9 +20,21 @@ constexpr int kGatherUnroll = 8;                   // 16-byte loads in flight pe
 
 constexpr int kMaxSlots = 65535;                   // slot ids are kept as uint16 in shared memory
 constexpr int kMaxRequests = 1 << 20;        // requests per context
-constexpr uint32_t kSpinLimit = 1u << 21;          // bounded waits on a request's flags
 constexpr unsigned kPollSleepNs = 32;              // first pause between polls of a flag,
 constexpr unsigned kPollSleepMaxNs = 256;          // doubling up to this (fewer polls, less L2 traffic)
+// Every device wait gives up once the waiting CTA has run this long (global-timer
+// nanoseconds from the CTA's start), records HS_STATUS_TIMEOUT and returns. A healthy
+// wait lasts microseconds; the limit only bounds a lost hand-off (hs_set_wait_limit).
+constexpr uint64_t kDefaultWaitNs = 20000000ull;   // 20 ms
+constexpr uint64_t kMinWaitNs = 1000ull;
+constexpr uint64_t kMaxWaitNs = 10000000000ull;    // 10 s
+
+// The global timer (nanoseconds); the clock every bounded wait is measured on.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 // Everything the two kernels need about one context.
 // Replacement policies (values of HS_POLICY_*).
@@ -53,6 +65,10 @@ struct Layout {
     int32_t* jslot = nullptr;
     int policy = kPolicyLru;  // replacement policy of the calls launched with this layout
     uint64_t seed = 0;        // kPolicyRandom's seed
+    uint64_t wait_ns = kDefaultWaitNs;  // time limit of every device wait of a CTA
+    // fault injection for tests (HS_FLAG_TEST_STALL): the resolution publishes nothing,
+    // so a fetch grid waiting on its flags runs out of time
+    int no_publish = 0;
 };
 
 // Bytes of the miss area for R requests of S slots, and its layout at `base`
@@ -102,9 +118,11 @@ constexpr int kAttendMaxHeads = 128;
 size_t attend_smem_bytes();
 AttendPlan attend_plan(int B, int H, int k, int num_sms);
 cudaError_t configure_attend();
+// `stall` (tests only): the producers withhold their first fill, so the MMA thread's
+// wait for it runs out of time and the kernel takes its abort path.
 cudaError_t launch_attend(const Layout& L, cudaStream_t stream, const uint16_t* q, int B, int H,
                           const int32_t* out_slots, int k, float sm_scale, float* o, float* lse,
-                          void* workspace, const AttendPlan& plan);
+                          void* workspace, const AttendPlan& plan, bool stall = false);
 
 // Set the calling thread's message for hs_last_error().
 void record_error(const char* msg);

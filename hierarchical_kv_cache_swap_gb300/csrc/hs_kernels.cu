@@ -36,8 +36,9 @@
 // 0's counter of its request and tags the call's flags with counter + 1. A flag left
 // from an earlier call never carries the tag a later fetch waits for (calls without a
 // fetch publish nothing and advance nothing), and graph replays need no host reset.
-// Every wait is bounded: on expiry
-// the CTA records HS_STATUS_TIMEOUT and skips, so no wait can hang the GPU.
+// Every wait is bounded in time (global timer, the context's wait limit counted from the
+// CTA's start): on expiry the CTA records HS_STATUS_TIMEOUT and skips, so no wait can
+// hang the GPU.
 //
 // No tensor cores: nothing here is a contraction.
 #include <cuda_runtime.h>
@@ -101,20 +102,22 @@ __device__ __forceinline__ void publish(uint32_t* flag, uint32_t value, bool on)
     if (threadIdx.x == 0) st_release(flag, value);
 }
 
-// Thread 0 waits (bounded) until (*flag & mask) == want and broadcasts the flag's
-// value; the outcome is block-uniform. On expiry the wait records HS_STATUS_TIMEOUT
-// and returns false.
-__device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t want, uint32_t mask,
+// Thread 0 waits until (*flag & mask) == want and broadcasts the flag's value; the
+// outcome is block-uniform. The wait gives up once the global timer passes `deadline`
+// (the CTA's start plus the context's wait limit): it then records HS_STATUS_TIMEOUT
+// and returns false. Polls back off from 32 to 256 ns.
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t want, uint32_t mask, uint64_t deadline,
                                           uint32_t* status, uint32_t* bcast, uint32_t* value) {
     if (threadIdx.x == 0) {
         uint32_t ok = 1, it = 0, v;
         while (((v = ld_acquire(flag)) & mask) != want) {
-            if (++it > kSpinLimit) {
+            if (global_ns() > deadline) {
                 ok = 0;
                 atomicOr(status, HS_STATUS_TIMEOUT);
                 break;
             }
             __nanosleep(min(kPollSleepNs << min(it, 4u), kPollSleepMaxNs));  // backing off
+            ++it;
         }
         bcast[0] = ok;
         bcast[1] = v;
@@ -543,8 +546,9 @@ resolve_kernel(const Layout L, const int32_t* __restrict__ sel, int k, int32_t* 
     // the call's stamp and tag (read once by every thread; both only change between calls)
     const int32_t t0 = *(volatile const int32_t*)(L.step + b);
     const uint32_t ready = ld_relaxed(L.gcount + b) + 1u;
-    // Flags are raised only when a fetch grid follows (it advances the counters).
-    const bool pub = fetch != 0;
+    // Flags are raised only when a fetch grid follows (it advances the counters) and
+    // no stall is being injected.
+    const bool pub = fetch != 0 && !L.no_publish;
     // ready_pos carries the tag's low half in its high half and the miss count in its
     // low half, so a fetch CTA learns both from the one acquire load it waits on.
     const uint32_t tag = (ready & 0xffffu) << 16;
@@ -585,11 +589,13 @@ resolve_kernel(const Layout L, const int32_t* __restrict__ sel, int k, int32_t* 
 // One fetch CTA's share of request b: entries q, q + nq, q + 2nq, ... of its fetch
 // list (position p, selection index j); the row of p goes to slot out[b][j].
 __device__ __forceinline__ void fetch_rows(const Layout& L, const int32_t* out, int k, int b, uint32_t q,
-                                           uint32_t nq, uint32_t ready, bool sync, uint32_t* bcast) {
+                                           uint32_t nq, uint32_t ready, bool sync, uint64_t deadline,
+                                           uint32_t* bcast) {
     constexpr int GT = kGatherThreads;
     uint32_t v;
     if (sync) {
-        if (!wait_flag(L.ready_pos + b, (ready & 0xffffu) << 16, 0xffff0000u, L.status, bcast, &v)) return;
+        if (!wait_flag(L.ready_pos + b, (ready & 0xffffu) << 16, 0xffff0000u, deadline, L.status, bcast, &v))
+            return;
     } else {  // launched after the resolution: its hand-off is complete
         v = ld_relaxed(L.ready_pos + b);
     }
@@ -615,7 +621,7 @@ __device__ __forceinline__ void fetch_rows(const Layout& L, const int32_t* out, 
             }
         }
         if (!slots_known) {  // the loads above are in flight while the victims are ranked
-            if (sync && !wait_flag(L.ready_slot + b, ready, 0xffffffffu, L.status, bcast, &v)) return;
+            if (sync && !wait_flag(L.ready_slot + b, ready, 0xffffffffu, deadline, L.status, bcast, &v)) return;
             slots_known = true;
         }
 #pragma unroll
@@ -633,10 +639,10 @@ __device__ __forceinline__ void fetch_rows(const Layout& L, const int32_t* out, 
 // Request b's fetch by nq CTAs (this one is share q). The CTA's own counter for
 // (b, q) gives the call's tag and advances once the share is done.
 __device__ __forceinline__ void fetch_request(const Layout& L, const int32_t* out, int k, int b, uint32_t q,
-                                              uint32_t nq, bool sync, uint32_t* bcast) {
+                                              uint32_t nq, bool sync, uint64_t deadline, uint32_t* bcast) {
     uint32_t* count = L.gcount + b + (size_t)q * L.R;
     const uint32_t ready = ld_relaxed(count) + 1u;
-    fetch_rows(L, out, k, b, q, nq, ready, sync, bcast);
+    fetch_rows(L, out, k, b, q, nq, ready, sync, deadline, bcast);
     __syncthreads();
     if (threadIdx.x == 0) *count = ready;
 }
@@ -647,12 +653,13 @@ gather_kernel(const Layout L, const int32_t* __restrict__ out, int k, int sync) 
     // The next call's resolution may be scheduled once every fetch CTA is resident (it
     // waits for this grid to finish before it reads anything).
     pdl_launch_dependents();
+    const uint64_t deadline = global_ns() + L.wait_ns;  // every wait of this CTA ends by then
     const uint32_t G = gridDim.x, c = blockIdx.x, R = (uint32_t)L.R;
     if (G >= R) {  // several CTAs share each request
         const uint32_t b = c % R;
-        fetch_request(L, out, k, (int)b, c / R, (G - 1 - b) / R + 1, sync != 0, bcast);
+        fetch_request(L, out, k, (int)b, c / R, (G - 1 - b) / R + 1, sync != 0, deadline, bcast);
     } else {  // each CTA takes whole requests
-        for (uint32_t b = c; b < R; b += G) fetch_request(L, out, k, (int)b, 0, 1, sync != 0, bcast);
+        for (uint32_t b = c; b < R; b += G) fetch_request(L, out, k, (int)b, 0, 1, sync != 0, deadline, bcast);
     }
     // This grid ends only after the resolution it serves: a successor that waits for this
     // grid then also sees every table update of that resolution.

@@ -26,8 +26,8 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[HS_NOALLOC_SCRA
 constexpr int kMaxDevices = 64;
 
 struct DeviceSetup {
-    std::once_flag once;
-    cudaError_t err = cudaSuccess;
+    std::mutex lock;
+    bool ready = false;       // set only once every step below has succeeded
     void* scratch = nullptr;  // device address of g_noalloc_scratch on this device
     int num_sms = 0;
 };
@@ -38,18 +38,29 @@ int noalloc_fail(int code, const char* msg) {
     return code;
 }
 
-// Once per device, with that device current: the array's device address (host code
-// only sees a host-side stand-in under its name) and the kernels' shared-memory
-// opt-in.
+// Per device, with that device current: the array's device address (host code only
+// sees a host-side stand-in under its name) and the kernels' shared-memory opt-in. The
+// device counts as set up only after all of it succeeded; a failed attempt (a transient
+// error, or a first call made while a stream is being captured) leaves it unset, and
+// the next call tries again.
 cudaError_t setup_device(int dev, DeviceSetup** out) {
     DeviceSetup& d = g_setup[dev];
-    std::call_once(d.once, [&] {
-        d.err = cudaGetSymbolAddress(&d.scratch, g_noalloc_scratch);
-        if (d.err == cudaSuccess) d.err = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (d.err == cudaSuccess) d.err = hs::configure_kernels(dev);
-    });
+    std::lock_guard<std::mutex> guard(d.lock);
     *out = &d;
-    return d.err;
+    if (d.ready) return cudaSuccess;
+    void* p = nullptr;
+    int sms = 0;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = hs::configure_kernels(dev);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();  // do not leave the failure for the caller's next check
+        return e;
+    }
+    d.scratch = p;
+    d.num_sms = sms;
+    d.ready = true;
+    return cudaSuccess;
 }
 
 }  // namespace

@@ -66,10 +66,19 @@ typedef struct CUevent_st* hs_event_t;
 #define HS_STATUS_RANGE 1u    /* a selection was >= context_len */
 #define HS_STATUS_DUP 2u      /* a position appeared twice in one request's row */
 #define HS_STATUS_STEP_LIMIT 4u /* a request reached 2^31-1 calls; the call was skipped */
-#define HS_STATUS_TIMEOUT 8u    /* a fetch waited too long for its resolution (should not happen) */
+#define HS_STATUS_TIMEOUT 8u    /* a device wait ran past the wait limit and gave up (see
+                                   hs_set_wait_limit); the call's rows may be missing: hs_reset */
 
 /* flags (hs_set_flags) */
 #define HS_FLAG_NO_COPY 1u /* do all bookkeeping but skip the host->device row fetch */
+/* Fault injection for tests, never for production: with it, hs_resolve's resolution
+ * publishes nothing, so its overlapped fetch grid (contexts with num_requests <= the
+ * SM count) waits for flags that are never raised, and hs_attend's producers withhold
+ * their first fill, so its MMA issuer waits for a barrier that never completes. Every
+ * such wait runs out after the wait limit: the kernels set HS_STATUS_TIMEOUT and
+ * return, the context stays usable, and its cache contents are undefined until
+ * hs_reset. A fetch that would not wait is not launched at all under this flag. */
+#define HS_FLAG_TEST_STALL 2u
 
 /*
  * hs_create -- one layer's cache for num_requests requests (paper abstract: full KV
@@ -230,6 +239,19 @@ int hs_clear_status(hs_ctx* ctx);
 
 /* hs_set_flags -- HS_FLAG_* bits for later calls (0 restores the default). */
 int hs_set_flags(hs_ctx* ctx, unsigned flags);
+
+/*
+ * hs_set_wait_limit -- time limit, in nanoseconds of the GPU's global timer, of the
+ * device waits of the kernels enqueued after it returns (hs_resolve's fetch grid waits
+ * for its resolution's per-request flags; hs_attend's roles wait on shared-memory
+ * barriers). A CTA's waits give up once it has run that long since it started; the
+ * kernel then sets HS_STATUS_TIMEOUT and returns instead of spinning, so no lost
+ * hand-off can hold the GPU. Default 20 ms (a healthy wait lasts microseconds); range
+ * [1 us, 10 s]. Calls captured into a CUDA graph keep the limit they were captured
+ * with. Not a timeout of the call as a whole: drains of in-flight copies after an
+ * expiry take at most one more limit. Returns HS_OK or HS_ERR_INVALID.
+ */
+int hs_set_wait_limit(hs_ctx* ctx, uint64_t ns);
 
 /* replacement policies (hs_set_policy) */
 #define HS_POLICY_LRU 0    /* the method's: victims are the least recently used slots */

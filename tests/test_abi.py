@@ -73,6 +73,7 @@ def test_calls_on_null_context_fail_cleanly(lib):
     assert lib.hs_resolve(None, None, None, 1, 1, None, None) == hs.HS_ERR_INVALID
     assert lib.hs_resolve_host(None, None, None, 1, 1, None, None) == hs.HS_ERR_INVALID
     assert lib.hs_set_flags(None, 0) == hs.HS_ERR_INVALID
+    assert lib.hs_set_wait_limit(None, 1_000_000) == hs.HS_ERR_INVALID
     assert lib.hs_reset(None, None) == hs.HS_ERR_INVALID
     assert lib.hs_kernels_per_call(None) == hs.HS_ERR_INVALID
     assert lib.hs_host_kv(None) is None and lib.hs_host_stride(None) == 0
