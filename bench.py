@@ -284,7 +284,8 @@ def load_peaks() -> dict:
 
 
 def step_figures(w, step_ms, res_ms, gat_ms, miss, peak_h2d: float, K: int) -> dict:
-    """Per-step and per-kernel figures of one workload's timed steps (miss: [K][B] counts)."""
+    """Per-step and per-kernel figures of one workload's timed steps (miss: [K][B] counts).
+    The kernels' own durations come from the serialised pass (hs_resolve_profiled)."""
     peaks = load_peaks()
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
     hbm_src = "MEASURED_PEAKS.json hbm_gbs (of measured)" if "hbm_gbs" in peaks else "fallback 6.8 TB/s"
@@ -312,6 +313,8 @@ def step_figures(w, step_ms, res_ms, gat_ms, miss, peak_h2d: float, K: int) -> d
                                "hbm_frac": res_bytes / (res_total * 1e-3) / 1e9 / hbm_peak,
                                "hbm_peak_source": hbm_src},
             "overlap_saving_us_per_step": (res_total + gat_total - total_ms) / K * 1e3,
+            "how": "each kernel's duration from the serialised pass (hs_resolve_profiled: events "
+                   "before, between and after the two kernels)",
         },
     }
 

@@ -78,7 +78,6 @@ void carve_miss_area(Layout& L, void* base);
 
 // Dynamic shared memory of one request's resolution for (C, S).
 size_t resolve_smem_bytes(int C, int S);
-size_t gather_smem_bytes();
 
 // Opt the kernels in to the device's maximum dynamic shared memory (the current
 // device must be `device`); returns a CUDA error.

@@ -8,7 +8,7 @@
 // The step is two kernels that run concurrently, chained by programmatic dependent
 // launch (PDL) and synchronized per request through release/acquire flags:
 //
-// resolve_kernel -- one 512-thread CTA per request:
+// resolve_kernel -- one 512-thread CTA per request (resolve_role):
 //   1. probe the page table for every selected position; hits are stamped and
 //      answered in place, misses are marked in a shared position bitmap;
 //   2. the probe lists every missed selection (position, index j in the row) in the
@@ -22,15 +22,16 @@
 //      pair the r-th miss with the r-th victim and answer the missed selections; the
 //      answers name every row's slot, so they are PUBLISHED (ready_slot) before the
 //      page table, slot tokens and stamps are updated.
-// gather_kernel -- a persistent grid of one CTA per SM (held to 64 registers, so that it
-//   fits beside a resolution CTA), launched right behind the resolution (PDL) so that it
-//   is resident while the resolution runs. Each CTA owns
+// gather_kernel -- a persistent grid of one CTA per SM (fetch_role; held to 64 registers,
+//   so that it fits beside a resolution CTA), launched right behind the resolution (PDL)
+//   so that it is resident while the resolution runs. Each CTA owns
 //   a share of one request's fetch list: it waits for ready_pos, issues the 16-byte
 //   zero-copy loads of its rows from the mapped host store (coalesced, 8 in flight
 //   per thread), waits for ready_slot only when it has to store, and writes each row
 //   into the slot the resolution answered for it. The host-link transfer -- the only real cost of the step --
 //   thus overlaps the victim ranking and the table updates, and uses every SM's load
-//   slots, not just the CTAs of the requests.
+//   slots, not just the CTAs of the requests. With more requests than SMs the
+//   resolution fills the GPU, and the fetch grid runs after it instead.
 // Flags carry a per-request call tag: each fetch CTA keeps a private counter for each
 // (request, share) it serves and advances it once per call; the resolution reads share
 // 0's counter of its request and tags the call's flags with counter + 1. A flag left
@@ -223,10 +224,10 @@ struct Request {
     int g0 = 0, g1 = 0, s0 = 0, s1 = 0;  // this thread's miss-bitmap groups and slot range
     const uint16_t* victims = nullptr;  // victims[r] = slot of the r-th miss
 
-    __device__ Request(const Layout& L_, const Plan& P_, uint8_t* smem_, const int32_t* sel, int k_,
+    __device__ Request(const Layout& L_, const Plan& P_, uint8_t* smem_, int b_, const int32_t* sel, int k_,
                        int32_t* out)
-        : L(L_), P(P_), smem(smem_), b(blockIdx.x), k(k_),
-          lim(L_.row_len ? __ldg(L_.row_len + blockIdx.x) : L_.C) {
+        : L(L_), P(P_), smem(smem_), b(b_), k(k_),
+          lim(L_.row_len ? __ldg(L_.row_len + b_) : L_.C) {
         selb = sel + (size_t)b * k;
         outb = out + (size_t)b * k;
         ptb = L.pt + (size_t)b * L.C;
@@ -530,25 +531,19 @@ struct Request {
     }
 };
 
-__global__ void __launch_bounds__(kResolveThreads, 2)
-resolve_kernel(const Layout L, const int32_t* __restrict__ sel, int k, int32_t* __restrict__ out,
-               int32_t* __restrict__ miss_counts, int fetch) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    // Launched as a programmatic dependent of the previous call's fetch grid: nothing is
-    // read before that grid (and, through its own wait, the previous resolution) is done.
-    pdl_wait_prerequisites();
-    pdl_launch_dependents();  // the fetch grid may start now; it synchronizes per request
-    const int b = blockIdx.x;
+// The resolution of request b by one CTA. With `pub` (fetch CTAs serve this call) it
+// publishes the request's fetch list after the probe and the answers once the victims
+// are chosen.
+__device__ __forceinline__ void resolve_role(const Layout& L, uint8_t* smem, int b, const int32_t* __restrict__ sel,
+                                             int k, int32_t* __restrict__ out, int32_t* __restrict__ miss_counts,
+                                             bool pub) {
     const Plan P(L.C, L.S);
-    Request R(L, P, smem, sel, k, out);
+    Request R(L, P, smem, b, sel, k, out);
     int32_t p[4], s[4];
     R.load_batch(0, p, s);
     // the call's stamp and tag (read once by every thread; both only change between calls)
     const int32_t t0 = *(volatile const int32_t*)(L.step + b);
     const uint32_t ready = ld_relaxed(L.gcount + b) + 1u;
-    // Flags are raised only when a fetch grid follows (it advances the counters) and
-    // no stall is being injected.
-    const bool pub = fetch != 0 && !L.no_publish;
     // ready_pos carries the tag's low half in its high half and the miss count in its
     // low half, so a fetch CTA learns both from the one acquire load it waits on.
     const uint32_t tag = (ready & 0xffffu) << 16;
@@ -647,20 +642,45 @@ __device__ __forceinline__ void fetch_request(const Layout& L, const int32_t* ou
     if (threadIdx.x == 0) *count = ready;
 }
 
-__global__ void __launch_bounds__(kGatherThreads, 2)  // <= 64 registers: fits beside a resolution CTA
+// Fetch CTA c of G: with G >= R, CTAs c = b (mod R) share request b's list; with fewer,
+// each takes whole requests in turn.
+__device__ __forceinline__ void fetch_role(const Layout& L, const int32_t* out, int k, uint32_t c, uint32_t G,
+                                           bool sync, uint32_t* bcast) {
+    const uint64_t deadline = global_ns() + L.wait_ns;  // every wait of this CTA ends by then
+    const uint32_t R = (uint32_t)L.R;
+    if (G >= R) {  // several CTAs share each request
+        const uint32_t b = c % R;
+        fetch_request(L, out, k, (int)b, c / R, (G - 1 - b) / R + 1, sync, deadline, bcast);
+    } else {  // each CTA takes whole requests
+        for (uint32_t b = c; b < R; b += G) fetch_request(L, out, k, (int)b, 0, 1, sync, deadline, bcast);
+    }
+}
+
+// The resolution of a call: one CTA per request. Launched as a programmatic dependent of
+// the previous call's fetch grid: nothing is read before that grid (and, through its own
+// wait, the previous resolution) is done.
+__global__ void __launch_bounds__(kResolveThreads, 2)
+resolve_kernel(const Layout L, const int32_t* __restrict__ sel, int k, int32_t* __restrict__ out,
+               int32_t* __restrict__ miss_counts, int fetch) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    pdl_wait_prerequisites();
+    pdl_launch_dependents();  // the fetch grid may start now; it synchronizes per request
+    // Flags are raised only when a fetch grid follows (it advances the counters) and no
+    // stall is being injected.
+    resolve_role(L, smem, (int)blockIdx.x, sel, k, out, miss_counts, fetch != 0 && !L.no_publish);
+}
+
+// The fetch of a call, held to 64 registers so that it is resident beside a resolution CTA
+// from the start. With `sync` it is a programmatic dependent of the resolution and waits
+// for each request's flags; without, it runs after the resolution and reads the hand-off
+// as it is.
+__global__ void __launch_bounds__(kGatherThreads, 2)
 gather_kernel(const Layout L, const int32_t* __restrict__ out, int k, int sync) {
     __shared__ uint32_t bcast[2];
     // The next call's resolution may be scheduled once every fetch CTA is resident (it
     // waits for this grid to finish before it reads anything).
     pdl_launch_dependents();
-    const uint64_t deadline = global_ns() + L.wait_ns;  // every wait of this CTA ends by then
-    const uint32_t G = gridDim.x, c = blockIdx.x, R = (uint32_t)L.R;
-    if (G >= R) {  // several CTAs share each request
-        const uint32_t b = c % R;
-        fetch_request(L, out, k, (int)b, c / R, (G - 1 - b) / R + 1, sync != 0, deadline, bcast);
-    } else {  // each CTA takes whole requests
-        for (uint32_t b = c; b < R; b += G) fetch_request(L, out, k, (int)b, 0, 1, sync != 0, deadline, bcast);
-    }
+    fetch_role(L, out, k, blockIdx.x, gridDim.x, sync != 0, bcast);
     // This grid ends only after the resolution it serves: a successor that waits for this
     // grid then also sees every table update of that resolution.
     pdl_wait_prerequisites();
@@ -669,8 +689,6 @@ gather_kernel(const Layout L, const int32_t* __restrict__ out, int k, int sync) 
 }  // namespace
 
 size_t resolve_smem_bytes(int C, int S) { return Plan(C, S).fixed; }
-
-size_t gather_smem_bytes() { return 0; }
 
 size_t miss_area_bytes(int R, int S, int num_sms) {
     const size_t list = ((size_t)R * S * 4 + 15) & ~(size_t)15;

@@ -5,19 +5,18 @@ host_to_device_ratio set HiSparse's working range (2048 / 6144 / 10 for a disagg
 decode instance). Reading taken: the host pool is host_to_device_ratio times the device
 pool, counted in entries (rows); the device pool is the requests' S-slot buffers; every
 admitted request reserves its whole history in the host pool.
+
+What one request costs on the device per layer is not restated here: it is whatever the
+library allocates, which a GPU test measures (cudaMemGetInfo around hs_create) and
+compares with the planner's figure. This restatement takes that figure as an input and
+checks the admission arithmetic built on it.
 """
 
 
 def plan(top_k, device_buffer_size, host_to_device_ratio, entry_bytes, layers, context_len,
-         hbm_bytes, host_bytes, miss_fraction, link_gbs):
+         hbm_bytes, host_bytes, miss_fraction, link_gbs, device_bytes_per_layer):
     S, C, L, E = device_buffer_size, context_len, layers, entry_bytes
-    # one request, one layer: its buffer, its page table over C positions, slot tokens and
-    # stamps (4 bytes each per slot), its miss list (position and index, 4 bytes each per
-    # slot), the device copy of the missed selections' answers that the fetch reads (4 bytes
-    # per slot), the host-call staging (selections and answers, 4 bytes each per slot) and
-    # 16 bytes of counters and flags
-    per_layer = S * E + 4 * C + 4 * S + 4 * S + 8 * S + 4 * S + 8 * S + 16
-    device_bytes = L * per_layer
+    device_bytes = L * device_bytes_per_layer
     by_device = hbm_bytes // device_bytes
     rows = min(int(host_to_device_ratio * by_device * S), host_bytes // (E * L))
     by_host = rows // C

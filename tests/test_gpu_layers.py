@@ -59,18 +59,24 @@ def test_consumer_checksum_equals_host_rows():
     ctx.close()
 
 
-def test_layerwise_prefetch_on_two_streams_equals_serial():
-    w = tracegen.WORKLOADS["quest"]
-    B, L, T = 4, w.L, 10
+def layerwise_equals_serial(w, B: int, T: int, stores: int) -> None:
+    """The two-stream order against the serial order over w.L layers sharing one selection:
+    outputs, states, device bytes and consumer checksums bit-identical, and every checksum
+    equal to the checksum of the host rows the selection names. The layers' contexts read
+    `stores` distinct host stores in turn (layer l reads store l mod stores)."""
+    L = w.L
     sel = tracegen.trace(w, T=T, B=B)
     sd = torch.from_numpy(sel).cuda()
     serial = []
     for layer in range(L):
-        c = hs.Context(B, w.C, w.S, w.E)
-        tracegen.fill_kv(c.host_kv_address(), c.host_stride, w, B=B, layer=layer)
+        if layer < stores:
+            c = hs.Context(B, w.C, w.S, w.E)
+            tracegen.fill_kv(c.host_kv_address(), c.host_stride, w, B=B, layer=layer)
+        else:
+            c = hs.Context(B, w.C, w.S, w.E, share_host_with=serial[layer % stores])
         serial.append(c)
     # the overlapped run's contexts read the same host stores (lent, not copied)
-    over = [hs.Context(B, w.C, w.S, w.E, share_host_with=serial[layer]) for layer in range(L)]
+    over = [hs.Context(B, w.C, w.S, w.E, share_host_with=serial[layer % stores]) for layer in range(L)]
 
     def buffers():
         return (torch.empty((T, L, B, w.k), dtype=torch.int32, device="cuda"),
@@ -102,12 +108,26 @@ def test_layerwise_prefetch_on_two_streams_equals_serial():
     for layer in range(L):
         for name in ("page_table", "slot_token", "last_use", "step", "device_kv"):
             assert torch.equal(getattr(serial[layer], name)(), getattr(over[layer], name)()), (layer, name)
+        assert serial[layer].status() == 0 and over[layer].status() == 0
     # every layer's consumer read exactly the host rows of the shared selection
     sums = sum_o.cpu().numpy().view(np.uint64)
     for layer in (0, L - 1):
-        host = serial[layer].host_kv()
+        host = serial[layer % stores].host_kv()
         for t in (0, T - 1):
             assert np.array_equal(sums[t, layer], host_checksums(host, sel[t])), (layer, t)
     assert int(miss_s[1:].sum()) > 0
-    for c in over + serial:
+    for c in over + serial[::-1]:
         c.close()
+
+
+def test_layerwise_prefetch_on_two_streams_equals_serial():
+    w = tracegen.WORKLOADS["quest"]
+    layerwise_equals_serial(w, B=4, T=10, stores=w.L)
+
+
+def test_layerwise_prefetch_full_batch():
+    """The Quest workload's full batch (64 requests x 8 layers, 64-KiB pages) for 16 steps.
+    Eight distinct 17.2 GB stores would need 137 GB of pinned host memory, so the layers
+    read two distinct stores in turn (bytes are opaque to the method)."""
+    w = tracegen.WORKLOADS["quest"]
+    layerwise_equals_serial(w, B=w.B, T=16, stores=2)

@@ -54,14 +54,18 @@ def test_long_context_full_size_sampled():
     run_and_compare(w, T=w.T, sample=sample, checkpoints=[0, 1, 31, w.T - 1])
 
 
-def test_quest_pages_eight_layers_reduced_batch():
-    """Quest-style 64-KiB pages, 8 layers (one context each) sharing every selection."""
+def test_quest_pages_eight_layers_full_size():
+    """Quest-style 64-KiB pages at full size: 64 requests x 4096 pages (17.2 GB of pinned
+    host KV per layer), 256-page buffers, k = 128, the whole 128-step trace, every request
+    compared. The 8 layers share every selection and are independent contexts, so they are
+    resolved one after the other, each over its own store, freed before the next."""
     w = tracegen.WORKLOADS["quest"]
-    B, T = 8, 48
+    B, T = w.B, w.T
     sel = tracegen.trace(w, T=T, B=B)
     for layer in range(w.L):
         run = DeviceRun(w, T, B=B, layer=layer, sel=sel)
-        run_and_compare(w, T=T, B=B, checkpoints=[0, 7, T - 1], layer=layer, run=run)
+        stats = run_and_compare(w, T=T, B=B, checkpoints=[0, 7, T - 1], layer=layer, run=run)
+        assert stats["misses"].sum() > 0
         run.close()
 
 
@@ -274,6 +278,29 @@ def test_host_buffer_entry_point_matches_device_entry_point(sel_pinned, out_pinn
         assert np.array_equal(out, a.out_dev[t].cpu().numpy())
         assert np.array_equal(miss, a.miss_dev[t].cpu().numpy())
     assert torch.equal(a.ctx.device_kv(), b.device_kv())
+    a.close()
+    b.close()
+
+
+@pytest.mark.parametrize("B", [32, 200])
+def test_serialised_kernels_equal_the_overlapped_ones(B):
+    """hs_resolve overlaps its two kernels when there are at most as many requests as SMs
+    (the fetch waits for each request's flags) and runs them one after the other beyond;
+    the per-kernel timing entry point always runs them one after the other, with events
+    between. Every way must give the oracle's results."""
+    w = tracegen.Workload("split", 14, B=B, L=1, C=4096, S=512, k=256, E=64, kv_kind=tracegen.KV_RAW,
+                          T=12, keep_pct=80, zipf_s=1.1, seed=B)
+    a = DeviceRun(w, T=w.T)
+    run_and_compare(w, T=w.T, run=a, checkpoints=[0, w.T - 1])
+    b = DeviceRun(w, T=w.T)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for t in range(w.T):
+        b.ctx.resolve_profiled(b.sel_dev[t], b.out_dev[t], b.miss_dev[t], ev)
+    torch.cuda.synchronize()
+    assert b.ctx.status() == 0
+    assert torch.equal(a.out_dev, b.out_dev) and torch.equal(a.miss_dev, b.miss_dev)
+    for name in ("page_table", "slot_token", "last_use", "step", "device_kv"):
+        assert torch.equal(getattr(a.ctx, name)(), getattr(b.ctx, name)()), name
     a.close()
     b.close()
 
