@@ -21,7 +21,11 @@ constexpr int kGatherUnroll = 8;                   // 16-byte loads in flight pe
 constexpr int kMaxSlots = 65535;                   // slot ids are kept as uint16 in shared memory
 constexpr int kMaxRequests = 1 << 20;        // requests per context
 constexpr unsigned kPollSleepNs = 32;              // first pause between polls of a flag,
-constexpr unsigned kPollSleepMaxNs = 256;          // doubling up to this (fewer polls, less L2 traffic)
+constexpr unsigned kPollSleepMaxNs = 64;           // doubling up to this
+// A request's two hand-off flags each sit on a 128-byte line of their own (stride in
+// words): the fetch CTAs poll them while the resolution CTAs of other requests write
+// theirs, and flags sharing a line delayed each other by microseconds.
+constexpr int kFlagStride = 32;
 // Every device wait gives up once the waiting CTA has run this long (global-timer
 // nanoseconds from the CTA's start), records HS_STATUS_TIMEOUT and returns. A healthy
 // wait lasts microseconds; the limit only bounds a lost hand-off (hs_set_wait_limit).
@@ -55,8 +59,8 @@ struct Layout {
     // miss area, shared by the two kernels of a call (carve_miss_area):
     int32_t* fpos;         // [R][S]: fetch list -- positions of the missed selections
     int32_t* fsel;         // [R][S]: ... and their indices j in the row (list order is arbitrary)
-    uint32_t* ready_pos;   // [R]: (tag mod 2^16) << 16 | list length, once request b's list is published
-    uint32_t* ready_slot;  // [R]: == tag once request b's answers (out_slots) are written
+    uint32_t* ready_pos;   // [R][kFlagStride]: (tag mod 2^16) << 16 | list length, once request b's list is published
+    uint32_t* ready_slot;  // [R][kFlagStride]: == tag once request b's answers (out_slots) are written
     uint32_t* gcount;      // [R + G]: fetch CTA counters; (b, share q) at b + q*R; tag = gcount[b] + 1
     const int64_t* row_base = nullptr;  // [R] pooled store: first row of request b (else b * C)
     const int32_t* row_len = nullptr;   // [R] pooled store: positions request b has (else C)

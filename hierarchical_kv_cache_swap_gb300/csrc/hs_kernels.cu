@@ -93,6 +93,9 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
 __device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+__device__ __forceinline__ void st_relaxed(uint32_t* p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 // All threads' global writes so far become visible before *flag = value: the barrier
 // orders them before thread 0's release store, which is cumulative. Called by every
@@ -195,6 +198,15 @@ struct Plan {
     }
 };
 
+// Selections j0 + q*NT + tid (q < 4) of one request's row (-1 past its end).
+__device__ __forceinline__ void load_selections(const int32_t* __restrict__ selb, int k, int j0, int32_t (&p)[4]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int j = j0 + q * NT + (int)threadIdx.x;
+        p[q] = j < k ? __ldg(selb + j) : -1;
+    }
+}
+
 // One request's resolution state in shared memory, and the phases shared by both
 // kernels. Every phase is called by all threads of the CTA.
 struct Request {
@@ -274,21 +286,17 @@ struct Request {
         }
     }
 
-    // Loads the selections j0 + q*NT + tid (q < 4) and their page-table entries; with
-    // `extra`, also *extra_out = *extra, issued together with the selections.
-    __device__ __forceinline__ void load_batch(int j0, int32_t (&p)[4], int32_t (&s)[4],
-                                               const int32_t* extra = nullptr,
-                                               int32_t* extra_out = nullptr) const {
-        const int tid = threadIdx.x;
+    // The page-table entries of the selections p (this thread's batch).
+    __device__ __forceinline__ void load_slots(const int32_t (&p)[4], int32_t (&s)[4]) const {
         const int C = lim;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int j = j0 + q * NT + tid;
-            p[q] = j < k ? __ldg(selb + j) : -1;
-        }
-        if (extra) *extra_out = *(volatile const int32_t*)extra;
-#pragma unroll
         for (int q = 0; q < 4; ++q) s[q] = (p[q] >= 0 && p[q] < C) ? ptb[p[q]] : -1;
+    }
+
+    // Loads the selections j0 + q*NT + tid (q < 4) and their page-table entries.
+    __device__ __forceinline__ void load_batch(int j0, int32_t (&p)[4], int32_t (&s)[4]) const {
+        load_selections(selb, k, j0, p);
+        load_slots(p, s);
     }
 
     // The call is refused (the request reached its call limit): every selection -1.
@@ -536,34 +544,37 @@ struct Request {
 // are chosen.
 __device__ __forceinline__ void resolve_role(const Layout& L, uint8_t* smem, int b, const int32_t* __restrict__ sel,
                                              int k, int32_t* __restrict__ out, int32_t* __restrict__ miss_counts,
-                                             bool pub) {
+                                             bool pub, int32_t (&p)[4]) {
     const Plan P(L.C, L.S);
     Request R(L, P, smem, b, sel, k, out);
-    int32_t p[4], s[4];
-    R.load_batch(0, p, s);
+    int32_t s[4];
+    R.load_slots(p, s);  // p: the first batch of selections, already loaded
     // the call's stamp and tag (read once by every thread; both only change between calls)
     const int32_t t0 = *(volatile const int32_t*)(L.step + b);
     const uint32_t ready = ld_relaxed(L.gcount + b) + 1u;
     // ready_pos carries the tag's low half in its high half and the miss count in its
     // low half, so a fetch CTA learns both from the one acquire load it waits on.
     const uint32_t tag = (ready & 0xffffu) << 16;
-    uint32_t* rpos = L.ready_pos + b;
-    uint32_t* rslot = L.ready_slot + b;
+    uint32_t* rpos = L.ready_pos + (size_t)b * kFlagStride;
+    uint32_t* rslot = L.ready_slot + (size_t)b * kFlagStride;
     R.start();
     __syncthreads();  // bitmaps cleared
+    // With nothing to fetch the flags order nothing (the fetch reads no list and stores
+    // no row), so they are raised with plain stores: a release would first wait for this
+    // thread's earlier writes, a fence on the no-IO path.
     if (t0 == INT32_MAX) {  // refused: the request reached its call limit
         R.refuse(miss_counts);
         if (pub && threadIdx.x == 0) {
-            st_release(rpos, tag);
-            st_release(rslot, ready);
+            st_relaxed(rpos, tag);
+            st_relaxed(rslot, ready);
         }
         return;
     }
     R.t = t0;
     if (!R.probe(p, s)) {  // all hits: nothing to rank or fetch
         if (pub && threadIdx.x == 0) {
-            st_release(rpos, tag);
-            st_release(rslot, ready);
+            st_relaxed(rpos, tag);
+            st_relaxed(rslot, ready);
         }
         R.finish(miss_counts, 0);
         R.drain();
@@ -589,10 +600,10 @@ __device__ __forceinline__ void fetch_rows(const Layout& L, const int32_t* out, 
     constexpr int GT = kGatherThreads;
     uint32_t v;
     if (sync) {
-        if (!wait_flag(L.ready_pos + b, (ready & 0xffffu) << 16, 0xffff0000u, deadline, L.status, bcast, &v))
+        if (!wait_flag(L.ready_pos + (size_t)b * kFlagStride, (ready & 0xffffu) << 16, 0xffff0000u, deadline, L.status, bcast, &v))
             return;
     } else {  // launched after the resolution: its hand-off is complete
-        v = ld_relaxed(L.ready_pos + b);
+        v = ld_relaxed(L.ready_pos + (size_t)b * kFlagStride);
     }
     const uint32_t u = v & 0xffffu;  // entries in the fetch list
     const uint32_t cpr = (uint32_t)L.E >> 4;
@@ -616,7 +627,7 @@ __device__ __forceinline__ void fetch_rows(const Layout& L, const int32_t* out, 
             }
         }
         if (!slots_known) {  // the loads above are in flight while the victims are ranked
-            if (sync && !wait_flag(L.ready_slot + b, ready, 0xffffffffu, deadline, L.status, bcast, &v)) return;
+            if (sync && !wait_flag(L.ready_slot + (size_t)b * kFlagStride, ready, 0xffffffffu, deadline, L.status, bcast, &v)) return;
             slots_known = true;
         }
 #pragma unroll
@@ -657,17 +668,22 @@ __device__ __forceinline__ void fetch_role(const Layout& L, const int32_t* out, 
 }
 
 // The resolution of a call: one CTA per request. Launched as a programmatic dependent of
-// the previous call's fetch grid: nothing is read before that grid (and, through its own
-// wait, the previous resolution) is done.
+// the previous call's fetch grid. The selections are the caller's input, complete before
+// the call was enqueued (a kernel that writes them lets this one start only when it
+// finishes, or when it has signalled programmatic completion after writing them), so the
+// first batch is loaded before the wait; nothing the previous call writes is read before
+// that grid (and, through its own wait, the previous resolution) is done.
 __global__ void __launch_bounds__(kResolveThreads, 2)
 resolve_kernel(const Layout L, const int32_t* __restrict__ sel, int k, int32_t* __restrict__ out,
                int32_t* __restrict__ miss_counts, int fetch) {
     extern __shared__ __align__(16) uint8_t smem[];
+    int32_t p[4];
+    load_selections(sel + (size_t)blockIdx.x * k, k, 0, p);
     pdl_wait_prerequisites();
     pdl_launch_dependents();  // the fetch grid may start now; it synchronizes per request
     // Flags are raised only when a fetch grid follows (it advances the counters) and no
     // stall is being injected.
-    resolve_role(L, smem, (int)blockIdx.x, sel, k, out, miss_counts, fetch != 0 && !L.no_publish);
+    resolve_role(L, smem, (int)blockIdx.x, sel, k, out, miss_counts, fetch != 0 && !L.no_publish, p);
 }
 
 // The fetch of a call, held to 64 registers so that it is resident beside a resolution CTA
@@ -692,7 +708,7 @@ size_t resolve_smem_bytes(int C, int S) { return Plan(C, S).fixed; }
 
 size_t miss_area_bytes(int R, int S, int num_sms) {
     const size_t list = ((size_t)R * S * 4 + 15) & ~(size_t)15;
-    const size_t per = ((size_t)R * 4 + 15) & ~(size_t)15;
+    const size_t per = (size_t)R * kFlagStride * 4;
     const size_t counters = (size_t)R + (size_t)num_sms * kGatherCtasPerSm;  // >= R * ceil(G / R)
     return 2 * list + 2 * per + counters * 4;
 }
@@ -700,7 +716,7 @@ size_t miss_area_bytes(int R, int S, int num_sms) {
 void carve_miss_area(Layout& L, void* base) {
     uint8_t* p = static_cast<uint8_t*>(base);
     const size_t list = ((size_t)L.R * L.S * 4 + 15) & ~(size_t)15;
-    const size_t per = ((size_t)L.R * 4 + 15) & ~(size_t)15;
+    const size_t per = (size_t)L.R * kFlagStride * 4;
     L.fpos = reinterpret_cast<int32_t*>(p);
     L.fsel = reinterpret_cast<int32_t*>(p + list);
     p += 2 * list;

@@ -96,7 +96,7 @@ extern "C" int hs_resolve_noalloc(hs_stream_t stream, int num_requests, int cont
     if (area + sizeof(uint32_t) > HS_NOALLOC_SCRATCH_BYTES)
         return noalloc_fail(HS_ERR_LIMIT,
                             "num_requests * slots too large for the fixed scratch array "
-                            "(about 8*R*S + 12*R + 4*SMs bytes must fit in HS_NOALLOC_SCRATCH_BYTES)");
+                            "(about 8*R*S + 260*R + 4*SMs bytes must fit in HS_NOALLOC_SCRATCH_BYTES)");
     int dev = -1, optin = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return noalloc_fail(HS_ERR_CUDA, cudaGetErrorString(e));

@@ -115,10 +115,10 @@ int hs_plan(const hs_plan_params* in, hs_plan_result* out) {
     // device bytes of one request: per layer its S-slot buffer, its page table over the
     // context (4 B per position), slot tokens and stamps (8 B per slot), its miss list (8 B
     // per slot), the fetch's copy of the miss answers (4 B per slot), the staging of the
-    // host-buffer entry point (8 B per slot) and five 4-byte words (call counter, the two
-    // hand-off flags, the fetch's call counter, the staged miss count) -- what hs_create
-    // allocates per request, which a GPU test measures
-    const int64_t per_layer = S * E + 4 * C + 28 * S + 20;
+    // host-buffer entry point (8 B per slot), the two hand-off flags (a 128-byte line
+    // each) and three 4-byte words (call counter, the fetch's call counter, the staged
+    // miss count) -- what hs_create allocates per request, which a GPU test measures
+    const int64_t per_layer = S * E + 4 * C + 28 * S + 268;
     out->device_bytes_per_request = L * per_layer;
     out->requests_by_device = out->device_bytes_per_request > 0 ? in->hbm_bytes / out->device_bytes_per_request : 0;
     // the host pool is host_to_device_ratio times the device pool, in rows, clamped to the budget

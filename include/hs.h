@@ -88,8 +88,8 @@ typedef struct CUevent_st* hs_event_t;
  *   slots         S > 0 device slots per request (the GPU cache size)
  *   entry_bytes   E > 0 bytes per KV entry; a multiple of 16
  * Uses the calling thread's current CUDA device. Allocates everything up front
- * (R*C*E bytes of pinned host memory, R*S*E bytes of HBM, about 4*R*(C+6S+5) bytes of
- * tables, miss lists and staging); hs_resolve allocates nothing. Returns NULL on failure (HS_ERR_INVALID,
+ * (R*C*E bytes of pinned host memory, R*S*E bytes of HBM, 4*R*(C+7S) + 268*R bytes of
+ * tables, miss lists, flags and staging); hs_resolve allocates nothing. Returns NULL on failure (HS_ERR_INVALID,
  * HS_ERR_LIMIT, HS_ERR_NOMEM or HS_ERR_CUDA described by hs_last_error()). The caller
  * owns the handle and releases it with hs_destroy.
  */
@@ -122,8 +122,12 @@ hs_ctx* hs_create_with_host(int num_requests, int context_len, int slots, int en
  *                 bytes are at hs_device_kv() + ((size_t)b * S + slot) * E
  *   miss_counts   device int32 [B]: distinct missed positions of request b
  * The caller owns selections/out_slots/miss_counts and keeps them alive until the
- * enqueued work completes. Returns HS_OK, HS_ERR_INVALID (nothing enqueued) or
- * HS_ERR_CUDA (a launch failed).
+ * enqueued work completes. The call's first kernel is a programmatic dependent of the
+ * kernel before it on the stream and reads `selections` before waiting for that kernel:
+ * a kernel that writes the selections and uses programmatic dependent launch itself
+ * must signal completion to its dependents only after writing them (kernels that do not
+ * use it have finished before this call starts). Returns HS_OK, HS_ERR_INVALID (nothing
+ * enqueued) or HS_ERR_CUDA (a launch failed).
  */
 int hs_resolve(hs_ctx* ctx, hs_stream_t stream, const int32_t* selections, int B, int k,
                int32_t* out_slots, int32_t* miss_counts);
@@ -384,7 +388,7 @@ const char* hs_last_error(void);
  * the other (hs_resolve overlaps them). The miss list the two kernels
  * share lives in a fixed file-scope device array of HS_NOALLOC_SCRATCH_BYTES bytes,
  * which every GPU that loads this library keeps until the process exits; a call needs
- * about 8*R*S + 12*R + 4*G bytes of it, G = the GPU's SM count (up to 64 more for
+ * about 8*R*S + 260*R + 4*G bytes of it, G = the GPU's SM count (up to 64 more for
  * alignment) and larger sizes fail with
  * HS_ERR_LIMIT before anything is enqueued. Every call on a device shares that device's copy of the array, so calls
  * whose work overlaps on the GPU (on two streams, say) race: serialise them. The array

@@ -85,15 +85,15 @@ EXAMPLE = dict(top_k=2048, device_buffer_size=6144, host_to_device_ratio=10.0, e
 def test_plan_deployment_example_by_hand():
     """The disaggregated-decode knobs (top_k 2048, buffer 6144, ratio 10), a 61-layer model
     with 656-byte entries, 32k + 8k contexts, 100 GiB of HBM and 1500 GiB of pinned host
-    memory. By hand: per layer 6144*656 + 4*40960 + 28*6144 + 20 = 4,030,464 + 163,840 +
-    172,032 + 20 = 4,366,356 B, so 266,347,716 B per request and floor(107,374,182,400 /
-    266,347,716) = 403 requests by HBM; the pool wants 10*403*6144 = 24,760,320 rows and
+    memory. By hand: per layer 6144*656 + 4*40960 + 28*6144 + 268 = 4,030,464 + 163,840 +
+    172,032 + 268 = 4,366,604 B, so 266,362,844 B per request and floor(107,374,182,400 /
+    266,362,844) = 403 requests by HBM; the pool wants 10*403*6144 = 24,760,320 rows and
     1500 GiB holds floor(1,610,612,736,000 / (61*656)) = 40,249,218 rows, so 24,760,320
     rows = floor(604.5) = 604 histories of 40960 positions; 403 requests are admitted.
     (The per-layer device bytes are what hs_create allocates: measured on a GPU in
     tests/test_gpu_plan.py.)"""
     r = hs.plan(**EXAMPLE)
-    assert r["device_bytes_per_request"] == 266_347_716
+    assert r["device_bytes_per_request"] == 266_362_844
     assert r["requests_by_device"] == 403
     assert r["host_pool_rows"] == 24_760_320
     assert r["requests_by_host"] == 604
