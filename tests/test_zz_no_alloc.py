@@ -121,3 +121,50 @@ def test_noalloc_callers_with_separate_state_can_alternate():
     assert int(status.item()) == 0
     for ref in refs:
         ref.close()
+
+
+def test_noalloc_callers_of_different_sizes_can_alternate():
+    """Callers of different sizes share the library's scratch array, whose layout (the miss
+    lists, the per-request flags and the fetch counters) then shifts from one call to the
+    next. Two such callers -- 4 requests of 4096 slots and 24 requests of 2048 slots --
+    take turns, and every output, table and device byte must match hs_resolve on
+    contexts of the same sizes."""
+    hs.build()
+    tracegen.build()
+    lib = hs.load_library()
+    base = tracegen.WORKLOADS["dsa"]
+    T = 6
+    shapes = [dict(B=4, S=4096), dict(B=24, S=2048)]
+    callers = []
+    for i, sh in enumerate(shapes):
+        w = tracegen.Workload(f"size{i}", 20 + i, B=sh["B"], L=1, C=base.C, S=sh["S"], k=base.k, E=base.E,
+                              kv_kind=base.kv_kind, T=T, keep_pct=base.keep_pct, zipf_s=base.zipf_s,
+                              recent=base.recent, seed=40 + i)
+        ref = hs.Context(w.B, w.C, w.S, w.E)
+        tracegen.fill_kv(ref.host_kv_address(), ref.host_stride, w)
+        st = {
+            "pt": torch.full((w.B, w.C), -1, dtype=torch.int32, device="cuda"),
+            "tok": torch.full((w.B, w.S), -1, dtype=torch.int32, device="cuda"),
+            "lu": torch.full((w.B, w.S), -1, dtype=torch.int32, device="cuda"),
+            "step": torch.zeros(w.B, dtype=torch.int32, device="cuda"),
+            "dev": torch.zeros((w.B, w.S, w.E), dtype=torch.uint8, device="cuda"),
+        }
+        sel = torch.from_numpy(tracegen.trace(w, T=T)).cuda()
+        callers.append((w, ref, st, sel))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for t in range(T):
+        for w, ref, st, sel in callers:  # alternate sizes call after call
+            a_out, b_out = torch.empty_like(sel[t]), torch.full_like(sel[t], -7)
+            a_miss = torch.empty(w.B, dtype=torch.int32, device="cuda")
+            b_miss = torch.full((w.B,), -7, dtype=torch.int32, device="cuda")
+            ref.resolve(sel[t], a_out, a_miss)
+            rc = _noalloc(lib, w, ref.host_kv_address(), ref.host_stride, st, sel[t], b_out, b_miss, status)
+            assert rc == hs.HS_OK, hs.last_error()
+            torch.cuda.synchronize()
+            assert torch.equal(a_out, b_out) and torch.equal(a_miss, b_miss), (t, w.name)
+            for name, key in (("page_table", "pt"), ("slot_token", "tok"), ("last_use", "lu"), ("step", "step"),
+                              ("device_kv", "dev")):
+                assert torch.equal(getattr(ref, name)(), st[key]), (t, w.name, name)
+    assert int(status.item()) == 0
+    for _, ref, _, _ in callers:
+        ref.close()
