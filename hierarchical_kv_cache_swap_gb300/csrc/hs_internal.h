@@ -20,8 +20,6 @@ constexpr int kGatherUnroll = 8;                   // 16-byte loads in flight pe
 
 constexpr int kMaxSlots = 65535;                   // slot ids are kept as uint16 in shared memory
 constexpr int kMaxRequests = 1 << 20;        // requests per context
-constexpr unsigned kPollSleepNs = 32;              // first pause between polls of a flag,
-constexpr unsigned kPollSleepMaxNs = 64;           // doubling up to this
 // A request's two hand-off flags each sit on a 128-byte line of their own (stride in
 // words): the fetch CTAs poll them while the resolution CTAs of other requests write
 // theirs, and flags sharing a line delayed each other by microseconds.

@@ -109,19 +109,18 @@ __device__ __forceinline__ void publish(uint32_t* flag, uint32_t value, bool on)
 // Thread 0 waits until (*flag & mask) == want and broadcasts the flag's value; the
 // outcome is block-uniform. The wait gives up once the global timer passes `deadline`
 // (the CTA's start plus the context's wait limit): it then records HS_STATUS_TIMEOUT
-// and returns false. Polls back off from 32 to 256 ns.
+// and returns false. Polls follow one another without a pause: each flag has a line of
+// its own, and one polling thread per CTA costs less than the latency a pause adds.
 __device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t want, uint32_t mask, uint64_t deadline,
                                           uint32_t* status, uint32_t* bcast, uint32_t* value) {
     if (threadIdx.x == 0) {
-        uint32_t ok = 1, it = 0, v;
+        uint32_t ok = 1, v;
         while (((v = ld_acquire(flag)) & mask) != want) {
             if (global_ns() > deadline) {
                 ok = 0;
                 atomicOr(status, HS_STATUS_TIMEOUT);
                 break;
             }
-            __nanosleep(min(kPollSleepNs << min(it, 4u), kPollSleepMaxNs));  // backing off
-            ++it;
         }
         bcast[0] = ok;
         bcast[1] = v;
