@@ -424,6 +424,7 @@ def run_ours(args, rank: int, world: int, dist) -> None:
             if w.name != "dsa":
                 extras["dsa"] = measure_dsa(torch, hs, tracegen, flush, peak_h2d, W, K)
             extras["no_io"] = measure_noio(torch, hs, tracegen, flush)
+            extras["sweep"] = measure_sweep(torch, hs, tracegen, flush, peak_h2d)
             extras["quest_layerwise"] = layerwise(torch, hs, tracegen, tracegen.WORKLOADS["quest"],
                                                   W=4, K=16, rank=0, flush=flush, peak_h2d=peak_h2d)
         extras["clocks_extras"] = extra_sampler.summary()
@@ -791,6 +792,68 @@ def measure_append(torch, ctx, w, flush, n: int) -> dict:
     return {"calls": n, "rows_per_call": w.B, "link_bytes_per_call": link,
             "us_per_call": statistics.mean(us), "us_per_call_median": statistics.median(us),
             "link_gbs": link / (statistics.mean(us) * 1e-6) / 1e9}
+
+
+def measure_sweep(torch, hs, tracegen, flush, peak_h2d: float, W: int = 8, K: int = 16) -> dict:
+    """The buffer/locality sweep: 64 requests, context 65536, k = 2048, S in {2048, 4096,
+    6144} x keep in {50, 80, 95} %. Per point: misses per step and µs per layer-step with
+    the fetch (L2 flushed before each call) and without it (HS_FLAG_NO_COPY: the
+    bookkeeping alone, at that point's miss rate). The nine points share one host store
+    (its bytes depend only on the workload's seed)."""
+    lender = None
+    out = {}
+    ctxs = {}
+    try:
+        for S in (2048, 4096, 6144):
+            w0 = tracegen.sweep_workload(S, 50)
+            if lender is None:
+                lender = hs.Context(w0.B, w0.C, S, w0.E)
+                tracegen.fill_kv(lender.host_kv_address(), lender.host_stride, w0)
+                ctxs[S] = lender
+            else:
+                ctxs[S] = hs.Context(w0.B, w0.C, S, w0.E, share_host_with=lender)
+        stream = torch.cuda.current_stream()
+        for keep in (50, 80, 95):
+            for S in (2048, 4096, 6144):
+                w = tracegen.sweep_workload(S, keep)
+                T = W + K
+                sd = torch.from_numpy(tracegen.trace(w, T=T)).cuda()
+                o = torch.empty_like(sd)
+                m = torch.empty((T, w.B), dtype=torch.int32, device="cuda")
+                ctx = ctxs[S]
+                row = {}
+                for mode, flags in (("fetch", 0), ("bookkeeping_only", hs.HS_FLAG_NO_COPY)):
+                    ctx.set_flags(flags)
+                    ctx.reset()
+                    for t in range(W):
+                        ctx.resolve(sd[t], o[t], m[t])
+                    torch.cuda.synchronize()
+                    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                          for _ in range(K)]
+                    for i in range(K):
+                        flush.fill_(i & 0xFF)
+                        ev[i][0].record(stream)
+                        ctx.resolve(sd[W + i], o[W + i], m[W + i])
+                        ev[i][1].record(stream)
+                    torch.cuda.synchronize()
+                    row[mode] = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in ev)
+                ctx.set_flags(0)
+                misses = float(m[W:].sum()) / K
+                out[f"S{S}_keep{keep}"] = {
+                    "us_per_layer_step": row["fetch"], "us_per_layer_step_bookkeeping_only": row["bookkeeping_only"],
+                    "misses_per_step": misses, "resolutions_per_s": w.B / (row["fetch"] * 1e-6),
+                    "miss_fetch_frac_of_h2d_peak": misses * w.E / (row["fetch"] * 1e-6) / 1e9 / peak_h2d}
+        status = 0
+        for c in ctxs.values():
+            status |= c.status()
+    finally:
+        for S in (6144, 4096, 2048):
+            if S in ctxs:
+                ctxs[S].close()
+    return {"points": out, "steps": K, "warmup": W, "device_status": status,
+            "workload": "64 requests x 1 layer, context 65536, k=2048, 656-byte entries, Zipf(1.1) refill, seed 2",
+            "how": "per point: W warm-up + K timed steps from an empty cache, L2 flushed before each call; "
+                   "then the same with HS_FLAG_NO_COPY"}
 
 
 def run_noio(args, rank: int, world: int, dist) -> None:
