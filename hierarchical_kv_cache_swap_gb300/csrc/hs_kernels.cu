@@ -308,9 +308,19 @@ struct Request {
         drain();
     }
 
+    // The answers that need no ranking -- hits (stamped, not evictable) and padding or
+    // out-of-range selections -- are either written by the probe itself (`direct`) or by
+    // write_direct() after the hand-off flags: none of them is read by the fetch, and
+    // each flag's release waits for the writes before it. The caller chooses: deferred
+    // when the request's previous call had misses (so this one likely has too), direct
+    // otherwise (an all-hit call raises its flags without a release, and the probe's
+    // writes then drain under its barrier), and always direct when the selections take
+    // more than one batch (k > 4 * NT: they are no longer held in registers).
+    __device__ __forceinline__ bool one_batch() const { return k <= 4 * NT; }
+
     // 1. hit detection, starting from the batch already loaded into p/s (t set).
     // Returns true (block-uniform) if any selection missed.
-    __device__ bool probe(int32_t (&p)[4], int32_t (&s)[4]) {
+    __device__ bool probe(int32_t (&p)[4], int32_t (&s)[4], bool direct) {
         const int tid = threadIdx.x;
         const int C = lim;
         uint32_t st = 0;
@@ -325,8 +335,10 @@ struct Request {
                 if (ss >= 0) {  // hit: answered in place, stamped, not evictable
                     const uint32_t bit = 1u << (ss & 31);
                     if (atomicOr(&hitbm[ss >> 5], bit) & bit) st |= HS_STATUS_DUP;
-                    if (L.policy != kPolicyFifo) lub[ss] = t;  // FIFO keeps the fill call
-                    outb[j] = ss;
+                    if (direct) {
+                        if (L.policy != kPolicyFifo) lub[ss] = t;  // FIFO keeps the fill call
+                        outb[j] = ss;
+                    }
                 } else if (pp >= 0 && pp < C) {  // miss: marked, and listed for the fetch
                     const uint32_t bit = 1u << (pp & 31);
                     if (atomicOr(&posbm[pp >> 5], bit) & bit) st |= HS_STATUS_DUP;
@@ -336,12 +348,30 @@ struct Request {
                     fsel[e] = j;
                 } else {  // padding, or out of range
                     if (pp >= C) st |= HS_STATUS_RANGE;
-                    outb[j] = -1;
+                    if (direct) outb[j] = -1;
                 }
             }
         }
         if (st) atomicOr(L.status, st);
         return __syncthreads_or(any_miss) != 0;
+    }
+
+    // The hits' answers and stamps and the padding's -1 of this thread's batch, when the
+    // probe left them (one batch only; see one_batch). A hit slot is never a victim, so
+    // its stamp may land at any time during the call.
+    __device__ void write_direct(const int32_t (&p)[4], const int32_t (&s)[4], bool direct) {
+        if (direct) return;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int j = q * NT + threadIdx.x;
+            if (j >= k) continue;
+            if (s[q] >= 0) {
+                if (L.policy != kPolicyFifo) lub[s[q]] = t;  // FIFO keeps the fill call
+                outb[j] = s[q];
+            } else if (p[q] < 0 || p[q] >= lim) {
+                outb[j] = -1;
+            }
+        }
     }
 
     __device__ void drain() const { cp_async_wait_all(); }
@@ -541,9 +571,11 @@ struct Request {
 // The resolution of request b by one CTA. With `pub` (fetch CTAs serve this call) it
 // publishes the request's fetch list after the probe and the answers once the victims
 // are chosen.
+// `prev_all_hit`: the request's previous call had no miss, as far as its list flag tells
+// (a hint for where the hits' answers are written; see Request::one_batch).
 __device__ __forceinline__ void resolve_role(const Layout& L, uint8_t* smem, int b, const int32_t* __restrict__ sel,
                                              int k, int32_t* __restrict__ out, int32_t* __restrict__ miss_counts,
-                                             bool pub, int32_t (&p)[4]) {
+                                             bool pub, int32_t (&p)[4], bool prev_all_hit) {
     const Plan P(L.C, L.S);
     Request R(L, P, smem, b, sel, k, out);
     int32_t s[4];
@@ -551,6 +583,7 @@ __device__ __forceinline__ void resolve_role(const Layout& L, uint8_t* smem, int
     // the call's stamp and tag (read once by every thread; both only change between calls)
     const int32_t t0 = *(volatile const int32_t*)(L.step + b);
     const uint32_t ready = ld_relaxed(L.gcount + b) + 1u;
+    const bool direct = !R.one_batch() || prev_all_hit;
     // ready_pos carries the tag's low half in its high half and the miss count in its
     // low half, so a fetch CTA learns both from the one acquire load it waits on.
     const uint32_t tag = (ready & 0xffffu) << 16;
@@ -570,11 +603,12 @@ __device__ __forceinline__ void resolve_role(const Layout& L, uint8_t* smem, int
         return;
     }
     R.t = t0;
-    if (!R.probe(p, s)) {  // all hits: nothing to rank or fetch
+    if (!R.probe(p, s, direct)) {  // all hits: nothing to rank or fetch
         if (pub && threadIdx.x == 0) {
             st_relaxed(rpos, tag);
             st_relaxed(rslot, ready);
         }
+        R.write_direct(p, s, direct);
         R.finish(miss_counts, 0);
         R.drain();
         return;
@@ -587,6 +621,7 @@ __device__ __forceinline__ void resolve_role(const Layout& L, uint8_t* smem, int
     R.rank_victims();
     R.answer_misses(p);
     publish(rslot, ready, pub);  // the answers name the slots: the rows can be stored
+    R.write_direct(p, s, direct);
     R.apply();
     R.finish(miss_counts, R.m);
 }
@@ -678,11 +713,15 @@ resolve_kernel(const Layout L, const int32_t* __restrict__ sel, int k, int32_t* 
     extern __shared__ __align__(16) uint8_t smem[];
     int32_t p[4];
     load_selections(sel + (size_t)blockIdx.x * k, k, 0, p);
+    // The previous call's miss count, from its list flag: only a hint (a stale value costs
+    // time, not correctness), so it too is read before the wait.
+    const uint32_t prev = ld_relaxed(L.ready_pos + (size_t)blockIdx.x * kFlagStride);
     pdl_wait_prerequisites();
     pdl_launch_dependents();  // the fetch grid may start now; it synchronizes per request
     // Flags are raised only when a fetch grid follows (it advances the counters) and no
     // stall is being injected.
-    resolve_role(L, smem, (int)blockIdx.x, sel, k, out, miss_counts, fetch != 0 && !L.no_publish, p);
+    resolve_role(L, smem, (int)blockIdx.x, sel, k, out, miss_counts, fetch != 0 && !L.no_publish, p,
+                 (prev & 0xffffu) == 0);
 }
 
 // The fetch of a call, held to 64 registers so that it is resident beside a resolution CTA
