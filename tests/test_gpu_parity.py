@@ -128,6 +128,31 @@ def test_noio_all_hits_after_first_call():
     run.close()
 
 
+def test_calls_alternating_all_hit_and_missing_with_padding():
+    """Every selection row is resolved twice in a row, the second time in a new order with
+    some entries turned into padding: the repeat is all hits (or padding), and the next
+    call has hits, misses and padding after an all-hit call. Hits and padding are answered
+    either by the probe itself or after the hand-off flags, depending on the previous
+    call; both orders must give the oracle's results, tables and bytes."""
+    w = tracegen.WORKLOADS["dsa"]
+    B, T = 6, 12
+    base = tracegen.trace(w, T=T // 2, B=B)
+    rng = np.random.default_rng(17)
+    rows = []
+    for t in range(T // 2):
+        rows.append(base[t].copy())
+        rep = np.stack([rng.permutation(r) for r in base[t]])
+        rep[:, :rng.integers(0, 40)] = -1  # a few padding entries
+        rows.append(rep.astype(np.int32))
+    sel = np.stack(rows)
+    run = DeviceRun(w, T, B=B, sel=sel)
+    stats = run_and_compare(w, T=T, B=B, run=run, checkpoints=[0, 1, 5, T - 1])
+    miss = run.miss_dev.cpu().numpy()
+    assert (miss[1::2] == 0).all() and (miss[2::2] > 0).all()
+    assert stats["misses"].sum() > 0
+    run.close()
+
+
 @pytest.mark.parametrize("C,S,k,E,B", [
     (1, 1, 1, 16, 1),          # degenerate: one position, one slot
     (37, 5, 5, 16, 3),         # k = S, ragged bitmap words
