@@ -102,21 +102,34 @@ int check_call(hs_ctx* h, const void* sel, int B, int k, const void* out, const 
 
 int enqueue(hs_ctx* h, cudaStream_t s, const int32_t* sel, int k, int32_t* out, int32_t* miss,
             cudaEvent_t* ev) {
-    bool fetch = !(h->flags & HS_FLAG_NO_COPY);
-    // chained by programmatic dependent launch unless events sit between the kernels
-    const bool pdl = ev == nullptr && hs::overlap_fetch(h->L.R, h->num_sms);
-    // A stalled resolution publishes nothing. Only a fetch grid that waits for the flags
-    // (the overlapped one) may follow it: the others would read a stale hand-off.
+    const hs::Layout& L = h->L;
+    const bool fetch = !(h->flags & HS_FLAG_NO_COPY);
+    // A stalled resolution (tests) publishes nothing: only a fetch grid that waits for the
+    // flags may follow it; one that reads the hand-off as is would read a stale one.
     h->L.no_publish = (h->flags & HS_FLAG_TEST_STALL) ? 1 : 0;
-    if (h->L.no_publish && !pdl) fetch = false;
     cudaError_t e;
-    if (ev && (e = cudaEventRecord(ev[0], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    if ((e = hs::launch_resolve(h->L, s, sel, k, out, miss, fetch)) != cudaSuccess)
-        return cuda_fail(e, "resolution kernel launch");
-    if (ev && (e = cudaEventRecord(ev[1], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    if (fetch && (e = hs::launch_gather(h->L, s, out, k, h->num_sms, pdl)) != cudaSuccess)
-        return cuda_fail(e, "fetch kernel launch");
-    if (ev && (e = cudaEventRecord(ev[2], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if (ev || !fetch) {
+        // per-kernel timing (events before, between and after), or bookkeeping only: the
+        // resolution of every request in one grid, then (when fetching) the fetch after it
+        if (ev && (e = cudaEventRecord(ev[0], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        if ((e = hs::launch_resolve(L, s, sel, k, out, miss, fetch, 0, L.R, true)) != cudaSuccess)
+            return cuda_fail(e, "resolution kernel launch");
+        if (ev && (e = cudaEventRecord(ev[1], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        if (fetch && !L.no_publish && (e = hs::launch_gather(L, s, out, k, h->num_sms, false, 0, L.R)) != cudaSuccess)
+            return cuda_fail(e, "fetch kernel launch");
+        if (ev && (e = cudaEventRecord(ev[2], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    } else {
+        // chunks of at most num_sms requests, each resolution overlapped with its fetch
+        const int n = hs::chunk_count(L.R, h->num_sms);
+        for (int i = 0; i < n; ++i) {
+            int b0, nr;
+            hs::chunk_requests(L.R, n, i, &b0, &nr);
+            if ((e = hs::launch_resolve(L, s, sel, k, out, miss, true, b0, nr, i == 0)) != cudaSuccess)
+                return cuda_fail(e, "resolution kernel launch");
+            if ((e = hs::launch_gather(L, s, out, k, h->num_sms, true, b0, nr)) != cudaSuccess)
+                return cuda_fail(e, "fetch kernel launch");
+        }
+    }
     g_err[0] = 0;
     return HS_OK;
 }
@@ -522,8 +535,7 @@ int hs_set_policy(hs_ctx* h, int policy, uint64_t seed) {
 int hs_kernels_per_call(hs_ctx* h) {
     if (!h) return fail(HS_ERR_INVALID, "null context");
     if (h->flags & HS_FLAG_NO_COPY) return 1;
-    if ((h->flags & HS_FLAG_TEST_STALL) && !hs::overlap_fetch(h->L.R, h->num_sms)) return 1;
-    return 2;
+    return 2 * hs::chunk_count(h->L.R, h->num_sms);
 }
 
 }  // extern "C"

@@ -85,20 +85,30 @@ size_t resolve_smem_bytes(int C, int S);
 // device must be `device`); returns a CUDA error.
 cudaError_t configure_kernels(int device);
 
-// Enqueue the resolution kernel (one CTA per request). With `fetch` (a fetch grid is
-// enqueued next) it publishes each request's miss positions as soon as they are ranked
-// and the victim slots once chosen.
+// Enqueue the resolution of requests b0 .. b0 + nr - 1 (one CTA per request). With
+// `fetch` (a fetch grid for them is enqueued next) it publishes each request's miss
+// positions as soon as they are known and the victim slots once chosen. `wait` = false
+// only for a later chunk of a call's requests (see chunk_requests).
 cudaError_t launch_resolve(const Layout& L, cudaStream_t stream, const int32_t* sel, int k,
-                           int32_t* out_slots, int32_t* miss_counts, bool fetch);
+                           int32_t* out_slots, int32_t* miss_counts, bool fetch, int b0, int nr, bool wait);
 
-// Enqueue the row fetch (a persistent grid of kGatherCtasPerSm CTAs per SM). With
-// `pdl` it is chained to the preceding resolution by programmatic dependent launch and
-// runs concurrently with it, starting on each request's rows as soon as they are
-// published; without it, it runs after the resolution and reads the hand-off as is.
-// Overlap pays when the resolution leaves SMs free for the fetch grid.
-inline bool overlap_fetch(int R, int num_sms) { return R <= num_sms; }
+// Enqueue the row fetch of requests b0 .. b0 + nr - 1 (a persistent grid of
+// kGatherCtasPerSm CTAs per SM). With `pdl` it is chained to the preceding resolution by
+// programmatic dependent launch and runs concurrently with it, starting on each
+// request's rows as soon as they are published; without it, it runs after the
+// resolution and reads the hand-off as is.
 cudaError_t launch_gather(const Layout& L, cudaStream_t stream, const int32_t* out_slots, int k, int num_sms,
-                          bool pdl);
+                          bool pdl, int b0, int nr);
+
+// Chunks of a call: with more requests than SMs, the requests are resolved in
+// ceil(R / num_sms) chunks of at most num_sms requests, each followed by its fetch grid;
+// a chunk's resolution (one CTA per request, two per SM) then leaves room for its fetch
+// grid, and the next chunk's resolution runs under the previous chunk's fetch.
+inline int chunk_count(int R, int num_sms) { return R <= num_sms ? 1 : (R + num_sms - 1) / num_sms; }
+inline void chunk_requests(int R, int nchunks, int i, int* b0, int* nr) {
+    *b0 = (int)((long long)R * i / nchunks);
+    *nr = (int)((long long)R * (i + 1) / nchunks) - *b0;
+}
 
 // Enqueue the consumer stand-in: sums[b] = sum (mod 2^64) of the 8-byte words of the
 // k rows request b resolved to (slots < 0 skipped); zeroes sums first.

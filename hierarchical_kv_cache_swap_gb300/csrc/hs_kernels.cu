@@ -689,39 +689,45 @@ __device__ __forceinline__ void fetch_request(const Layout& L, const int32_t* ou
 
 // Fetch CTA c of G: with G >= R, CTAs c = b (mod R) share request b's list; with fewer,
 // each takes whole requests in turn.
+// Fetch CTA c of G serving requests b0 .. b0 + nr - 1: with G >= nr, CTAs c = i (mod nr)
+// share request b0 + i's list; with fewer, each takes whole requests in turn. Share q of
+// request b keeps its call counter at gcount[b + q * R].
 __device__ __forceinline__ void fetch_role(const Layout& L, const int32_t* out, int k, uint32_t c, uint32_t G,
-                                           bool sync, uint32_t* bcast) {
+                                           bool sync, uint32_t* bcast, uint32_t b0, uint32_t nr) {
     const uint64_t deadline = global_ns() + L.wait_ns;  // every wait of this CTA ends by then
-    const uint32_t R = (uint32_t)L.R;
-    if (G >= R) {  // several CTAs share each request
-        const uint32_t b = c % R;
-        fetch_request(L, out, k, (int)b, c / R, (G - 1 - b) / R + 1, sync, deadline, bcast);
+    if (G >= nr) {  // several CTAs share each request
+        const uint32_t i = c % nr;
+        fetch_request(L, out, k, (int)(b0 + i), c / nr, (G - 1 - i) / nr + 1, sync, deadline, bcast);
     } else {  // each CTA takes whole requests
-        for (uint32_t b = c; b < R; b += G) fetch_request(L, out, k, (int)b, 0, 1, sync, deadline, bcast);
+        for (uint32_t i = c; i < nr; i += G) fetch_request(L, out, k, (int)(b0 + i), 0, 1, sync, deadline, bcast);
     }
 }
 
-// The resolution of a call: one CTA per request. Launched as a programmatic dependent of
-// the previous call's fetch grid. The selections are the caller's input, complete before
-// the call was enqueued (a kernel that writes them lets this one start only when it
-// finishes, or when it has signalled programmatic completion after writing them), so the
-// first batch is loaded before the wait; nothing the previous call writes is read before
-// that grid (and, through its own wait, the previous resolution) is done.
+// The resolution of requests b0 .. b0 + gridDim.x - 1: one CTA per request. Launched as
+// a programmatic dependent of the preceding grid. The selections are the caller's input,
+// complete before the call was enqueued (a kernel that writes them lets this one start
+// only when it finishes, or when it has signalled programmatic completion after writing
+// them), so the first batch is loaded before the wait; nothing the previous call writes
+// is read before that grid (and, through its own wait, the previous resolution) is done.
+// A later chunk of a call's requests (`wait` = 0) does not wait: it is launched behind the
+// first chunk's fetch, which starts only once every CTA of the first chunk has passed its
+// wait -- the previous call is complete by then -- and its requests are disjoint from the
+// earlier chunks', so it runs under their fetch.
 __global__ void __launch_bounds__(kResolveThreads, 2)
 resolve_kernel(const Layout L, const int32_t* __restrict__ sel, int k, int32_t* __restrict__ out,
-               int32_t* __restrict__ miss_counts, int fetch) {
+               int32_t* __restrict__ miss_counts, int fetch, int b0, int wait) {
     extern __shared__ __align__(16) uint8_t smem[];
+    const int b = b0 + (int)blockIdx.x;
     int32_t p[4];
-    load_selections(sel + (size_t)blockIdx.x * k, k, 0, p);
+    load_selections(sel + (size_t)b * k, k, 0, p);
     // The previous call's miss count, from its list flag: only a hint (a stale value costs
     // time, not correctness), so it too is read before the wait.
-    const uint32_t prev = ld_relaxed(L.ready_pos + (size_t)blockIdx.x * kFlagStride);
-    pdl_wait_prerequisites();
+    const uint32_t prev = ld_relaxed(L.ready_pos + (size_t)b * kFlagStride);
+    if (wait) pdl_wait_prerequisites();
     pdl_launch_dependents();  // the fetch grid may start now; it synchronizes per request
     // Flags are raised only when a fetch grid follows (it advances the counters) and no
     // stall is being injected.
-    resolve_role(L, smem, (int)blockIdx.x, sel, k, out, miss_counts, fetch != 0 && !L.no_publish, p,
-                 (prev & 0xffffu) == 0);
+    resolve_role(L, smem, b, sel, k, out, miss_counts, fetch != 0 && !L.no_publish, p, (prev & 0xffffu) == 0);
 }
 
 // The fetch of a call, held to 64 registers so that it is resident beside a resolution CTA
@@ -729,12 +735,12 @@ resolve_kernel(const Layout L, const int32_t* __restrict__ sel, int k, int32_t* 
 // for each request's flags; without, it runs after the resolution and reads the hand-off
 // as it is.
 __global__ void __launch_bounds__(kGatherThreads, 2)
-gather_kernel(const Layout L, const int32_t* __restrict__ out, int k, int sync) {
+gather_kernel(const Layout L, const int32_t* __restrict__ out, int k, int sync, int b0, int nr) {
     __shared__ uint32_t bcast[2];
     // The next call's resolution may be scheduled once every fetch CTA is resident (it
     // waits for this grid to finish before it reads anything).
     pdl_launch_dependents();
-    fetch_role(L, out, k, blockIdx.x, gridDim.x, sync != 0, bcast);
+    fetch_role(L, out, k, blockIdx.x, gridDim.x, sync != 0, bcast, (uint32_t)b0, (uint32_t)nr);
     // This grid ends only after the resolution it serves: a successor that waits for this
     // grid then also sees every table update of that resolution.
     pdl_wait_prerequisites();
@@ -747,7 +753,11 @@ size_t resolve_smem_bytes(int C, int S) { return Plan(C, S).fixed; }
 size_t miss_area_bytes(int R, int S, int num_sms) {
     const size_t list = ((size_t)R * S * 4 + 15) & ~(size_t)15;
     const size_t per = (size_t)R * kFlagStride * 4;
-    const size_t counters = (size_t)R + (size_t)num_sms * kGatherCtasPerSm;  // >= R * ceil(G / R)
+    // share q of request b counts at b + q * R: a fetch grid of G = num_sms CTAs over a chunk
+    // of nr requests gives each request ceil(G / nr) shares at most, which is at most
+    // R + G counters in all when one chunk holds every request (R <= G) and at most 2R
+    // when chunks hold at least G / 2 requests each (R > G; see chunk_requests)
+    const size_t counters = (size_t)R + (size_t)(R > num_sms ? R : num_sms * kGatherCtasPerSm);
     return 2 * list + 2 * per + counters * 4;
 }
 
@@ -776,12 +786,12 @@ cudaError_t configure_kernels(int device) {
 }
 
 cudaError_t launch_resolve(const Layout& L, cudaStream_t stream, const int32_t* sel, int k,
-                           int32_t* out_slots, int32_t* miss_counts, bool fetch) {
+                           int32_t* out_slots, int32_t* miss_counts, bool fetch, int b0, int nr, bool wait) {
     // a programmatic dependent of whatever precedes it on the stream: it is scheduled early
     // only behind a grid that allows it (the previous call's fetch), and waits for that
     // grid's completion before its first read
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)L.R);
+    cfg.gridDim = dim3((unsigned)nr);
     cfg.blockDim = dim3(kResolveThreads);
     cfg.dynamicSmemBytes = resolve_smem_bytes(L.C, L.S);
     cfg.stream = stream;
@@ -790,11 +800,12 @@ cudaError_t launch_resolve(const Layout& L, cudaStream_t stream, const int32_t* 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, resolve_kernel, L, sel, k, out_slots, miss_counts, fetch ? 1 : 0);
+    return cudaLaunchKernelEx(&cfg, resolve_kernel, L, sel, k, out_slots, miss_counts, fetch ? 1 : 0, b0,
+                              wait ? 1 : 0);
 }
 
 cudaError_t launch_gather(const Layout& L, cudaStream_t stream, const int32_t* out_slots, int k, int num_sms,
-                          bool pdl) {
+                          bool pdl, int b0, int nr) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(num_sms * kGatherCtasPerSm));
     cfg.blockDim = dim3(kGatherThreads);
@@ -805,7 +816,7 @@ cudaError_t launch_gather(const Layout& L, cudaStream_t stream, const int32_t* o
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gather_kernel, L, out_slots, k, pdl ? 1 : 0);
+    return cudaLaunchKernelEx(&cfg, gather_kernel, L, out_slots, k, pdl ? 1 : 0, b0, nr);
 }
 
 }  // namespace hs

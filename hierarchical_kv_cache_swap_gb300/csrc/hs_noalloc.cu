@@ -121,12 +121,12 @@ extern "C" int hs_resolve_noalloc(hs_stream_t stream, int num_requests, int cont
     hs::carve_miss_area(L, base);
     L.status = status ? status : reinterpret_cast<uint32_t*>(base + area);
     cudaStream_t s = (cudaStream_t)stream;
-    if ((e = hs::launch_resolve(L, s, selections, k, out_slots, miss_counts, true)) != cudaSuccess)
+    if ((e = hs::launch_resolve(L, s, selections, k, out_slots, miss_counts, true, 0, R, true)) != cudaSuccess)
         return noalloc_fail(HS_ERR_CUDA, cudaGetErrorString(e));
     // Callers with different sizes share this array, so the fetch CTAs' call counters
     // need not line up with a caller's requests: the fetch therefore runs after the
     // resolution here (no overlap) and reads the hand-off without waiting on flags.
-    if ((e = hs::launch_gather(L, s, out_slots, k, d->num_sms, false)) != cudaSuccess)
+    if ((e = hs::launch_gather(L, s, out_slots, k, d->num_sms, false, 0, R)) != cudaSuccess)
         return noalloc_fail(HS_ERR_CUDA, cudaGetErrorString(e));
     hs::record_error("");
     return HS_OK;

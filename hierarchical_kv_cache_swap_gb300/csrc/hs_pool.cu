@@ -118,6 +118,7 @@ int hs_plan(const hs_plan_params* in, hs_plan_result* out) {
     // host-buffer entry point (8 B per slot), the two hand-off flags (a 128-byte line
     // each) and three 4-byte words (call counter, the fetch's call counter, the staged
     // miss count) -- what hs_create allocates per request, which a GPU test measures
+    // (with more requests than SMs a request keeps a second fetch counter: 4 B more)
     const int64_t per_layer = S * E + 4 * C + 28 * S + 268;
     out->device_bytes_per_request = L * per_layer;
     out->requests_by_device = out->device_bytes_per_request > 0 ? in->hbm_bytes / out->device_bytes_per_request : 0;
