@@ -49,6 +49,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="long")
+    ap.add_argument("--wait-limit-ms", type=float, default=None,
+                    help="device wait limit of the attention context (hs_set_wait_limit); a profiler's "
+                         "instrumented replays can run far slower than the default 20 ms allows")
     ap.add_argument("--no-extras", action="store_true",
                     help="only the headline workload: no CPU, DSA, no-IO, attention or layer-wise legs")
     return ap.parse_args()
@@ -220,7 +223,8 @@ def run_reference(args, rank: int, world: int) -> None:
     import oracle
     tracegen.build()
     oracle.build()
-    w = tracegen.noio_workload(4096) if args.workload == "noio" else tracegen.WORKLOADS[args.workload]
+    w = (tracegen.noio_workload(4096) if args.workload == "noio"
+         else tracegen.WORKLOADS["dsa" if args.workload == "attend" else args.workload])
     T = args.warmup + args.steps
     cores = host_cores()
     value, dt = oracle_rate(w, T, args.warmup, cores)
@@ -856,6 +860,48 @@ def measure_sweep(torch, hs, tracegen, flush, peak_h2d: float, W: int = 8, K: in
                    "then the same with HS_FLAG_NO_COPY"}
 
 
+def run_attend(args, rank: int, world: int, dist) -> None:
+    """The attention consumer as the headline: the DSA-style workload's resolved slots of one
+    step (32 requests x k = 2048), 128 heads, L2 flushed before each call."""
+    import torch
+
+    import __graft_entry__
+    import hierarchical_kv_cache_swap_gb300 as hs
+    import tracegen
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    __graft_entry__.build()
+    w = tracegen.WORKLOADS["dsa"]
+    T = 4
+    sd = torch.from_numpy(tracegen.trace(w, T=T)).cuda()
+    out = torch.empty_like(sd)
+    miss = torch.empty((T, w.B), dtype=torch.int32, device="cuda")
+    ctx = hs.Context(w.B, w.C, w.S, w.E)
+    if args.wait_limit_ms:
+        ctx.set_wait_limit(int(args.wait_limit_ms * 1e6))
+    tracegen.fill_kv(ctx.host_kv_address(), ctx.host_stride, w)
+    for t in range(T):
+        ctx.resolve(sd[t], out[t], miss[t])
+    torch.cuda.synchronize()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    with ClockSampler(local) as sampler:
+        att = measure_attend(torch, ctx, w, out[T - 1], flush, n=args.steps)
+    ctx.close()
+    us = att["us_per_call"]
+    line = {
+        "metric": METRIC, "value": weak_scaling_value(world, w.B, 1, us * 1e-3), "unit": UNIT + " (attention calls)",
+        "n_gpus": world, "steps": args.steps, "warmup": 3, "ms_per_step": us * 1e-3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": describe(w) + f"; attention over one step's resolved slots, {ATTEND_HEADS} heads",
+                   "l2": f"flushed before each call ({FLUSH_BYTES >> 20} MiB write)",
+                   "timing": "CUDA events around each hs_attend call"},
+        "attend": att, "roofline": att["roofline"], "clocks": sampler.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_noio(args, rank: int, world: int, dist) -> None:
     """The no-IO gate as the headline: 64 requests x k = 2048 over 4096 slots, every call all
     hits, back to back in a CUDA graph (and, apart, each call after an L2 flush)."""
@@ -1023,6 +1069,8 @@ def main():
             run_layers(args, rank, world, dist)
         elif args.workload == "noio":
             run_noio(args, rank, world, dist)
+        elif args.workload == "attend":
+            run_attend(args, rank, world, dist)
         else:
             run_ours(args, rank, world, dist)
     finally:
