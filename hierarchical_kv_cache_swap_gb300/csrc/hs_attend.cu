@@ -25,14 +25,18 @@
 //     instruction, 36 per block) into 256 TMEM columns, and O += P V (M=128, N=256 value
 //     dims, K=16 keys, 16 per block) with P read from TMEM; completion is signalled through
 //     mbarriers by tcgen05.commit. The widest N keeps the tensor core busy: an M=128
-//     instruction costs about the same whatever N is.
+//     instruction takes ~200 cycles whatever N is (measured from N=32 to 256).
 //   * 8 softmax warps in two groups of 128 keys (thread = head = TMEM lane in both) read
 //     S, keep a running maximum m (log2 domain) that moves only when a block's maximum
 //     exceeds it by more than 8 -- then O (in TMEM) and the running sums are rescaled --
 //     and write P = 2^(x - m) as bf16 over the scores already read; at the end they
-//     normalise O and write it with lse.
+//     normalise O and write it with lse. Each group signals each half of its keys (64)
+//     as soon as their P is written, and the product over those keys starts then, so
+//     the P V MMAs run under the rest of the softmax.
 // With several key splits per request each CTA writes its normalised partial and its
-// lse; combine_kernel merges them (weights exp(lse_s - lse)).
+// lse; combine_kernel merges them (weights exp(lse_s - lse)). It is launched as a
+// programmatic dependent of attend_kernel, so its launch overlaps the attention and
+// its blocks wait (griddepcontrol.wait) only for the attention's results.
 //
 // Every wait on an mbarrier is bounded in time (global timer, the context's wait limit
 // counted from the CTA's start): on expiry the CTA records HS_STATUS_TIMEOUT, every role
@@ -74,9 +78,9 @@ constexpr int kMaxSplitKeys = 2048;        // slots of one split staged in share
 
 // barrier indices
 enum { kFull = 0 /* kStages: producers' fills */, kFree = 4 /* kStages: MMAs done with a stage */,
-       kQLand = 8 /* kStages: a stage's Q chunk has landed */, kSFull = 12, kPFull = 13, kPvDone = 14,
-       kVmFull = 15 /* 2, by block parity */, kDrain = 17, kBmax = 18 /* 2, by block parity */, kLsum = 20,
-       kBars = 21 };
+       kQLand = 8 /* kStages: a stage's Q chunk has landed */, kSFull = 12, kPvDone = 13,
+       kVmFull = 14 /* 2, by block parity */, kDrain = 16, kBmax = 17 /* 2, by block parity */, kLsum = 19,
+       kPHalf = 20 /* 4: [softmax group][first or second half of its keys]: P written */, kBars = 24 };
 static_assert(kFree == kFull + kStages && kQLand == kFree + kStages && kSFull == kQLand + kStages, "barrier map");
 
 struct Smem {  // beyond Q and the stages
@@ -261,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
     const int kend = min(A.k, kbeg + A.keys_per_split);
     const int nb = kend > kbeg ? (kend - kbeg + kBlk - 1) / kBlk : 0;
     const uint64_t deadline = global_ns() + A.wait_ns;  // every wait of this CTA ends by then
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (tid == 0) {
         for (int st = 0; st < kStages; ++st) {
@@ -271,12 +276,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
         bar_init(&sm->bar[kVmFull], kBlk / 32);
         bar_init(&sm->bar[kVmFull + 1], kBlk / 32);
         bar_init(&sm->bar[kSFull], 1);
-        bar_init(&sm->bar[kPFull], kSoftWarps * 32);
         bar_init(&sm->bar[kPvDone], 1);
         bar_init(&sm->bar[kDrain], 1);
         bar_init(&sm->bar[kBmax], kSoftWarps * 32);
         bar_init(&sm->bar[kBmax + 1], kSoftWarps * 32);
         bar_init(&sm->bar[kLsum], kSoftWarps * 32);
+        for (int j = 0; j < 4; ++j) bar_init(&sm->bar[kPHalf + j], kSoftWarps / 2 * 32);
         sm->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -460,19 +465,23 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
                 }
                 if (!ok) break;
                 mma_commit(&sm->bar[kSFull]);
-                if (!bar_wait(sm, &sm->bar[kPFull], i & 1, A.status, deadline)) { ok = false; break; }
-                fence_after();
-                for (int vc = 0; vc < kVFills; ++vc, ++g) {
-                    const int st = g % kStages;
-                    if (!bar_wait(sm, &sm->bar[kFull + st], (g / kStages) & 1, A.status, deadline)) { ok = false; break; }
+                // P V in the order the softmax writes its halves: keys 0-63 and 128-191 (the
+                // first half of each group's keys), then 64-127 and 192-255
+                for (int j = 0; j < kVFills; ++j) {
+                    const int vc = (j >> 1) | ((j & 1) << 1);  // 0, 2, 1, 3
+                    if (!bar_wait(sm, &sm->bar[kPHalf + (vc >> 1) * 2 + (vc & 1)], i & 1, A.status, deadline)) { ok = false; break; }
+                    const uint32_t gv = g + (uint32_t)vc;
+                    const int st = gv % kStages;
+                    if (!bar_wait(sm, &sm->bar[kFull + st], (gv / kStages) & 1, A.status, deadline)) { ok = false; break; }
                     fence_after();
                     const uint32_t vb = s0 + st * kSlotBytes + kQChunk;
 #pragma unroll
                     for (int ks = 0; ks < kVKeys / 16; ++ks)
                         mma_ts(tmem + kColO, tmem + kColS + (kVKeys / 2) * vc + 8 * ks + (vc >= kVFills / 2 ? 64 : 0),
-                               smem_desc(vb + ks * 2048, kVSub, 1024), id_o, (i > 0 || vc > 0 || ks > 0) ? 1u : 0u);
+                               smem_desc(vb + ks * 2048, kVSub, 1024), id_o, (i > 0 || j > 0 || ks > 0) ? 1u : 0u);
                     mma_commit(&sm->bar[kFree + st]);
                 }
+                g += kVFills;
                 if (!ok) break;
                 mma_commit(&sm->bar[kPvDone]);
             }
@@ -552,10 +561,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
                     pk[c] = *reinterpret_cast<const uint32_t*>(&pb);
                 }
                 HS_ST16(tmem + lrow + kColS + 16 * ch + 64 * grp, pk);
+                if (ch & 1) {  // 64 keys written: their part of P V may start
+                    tmem_wait_st();
+                    fence_before();
+                    bar_arrive(&sm->bar[kPHalf + 2 * grp + ((ch >> 1) & 1)]);
+                }
             }
-            tmem_wait_st();
-            fence_before();
-            bar_arrive(&sm->bar[kPFull]);
         }
         // the running sum is the two groups' parts
         sm->lsum[grp][h] = l;
@@ -609,6 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
 __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                                                       int nsplit, int H, float* __restrict__ o, float* __restrict__ lse) {
     const int bh = blockIdx.x, b = bh / H, h = bh - b * H;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     float mx = -INFINITY;
     for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, part_lse[((size_t)b * nsplit + s) * H + h]);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -726,7 +738,17 @@ cudaError_t launch_attend(const Layout& L, cudaStream_t stream, const uint16_t* 
     attend_kernel<<<B * plan.nsplit * 2, kThreads, kSmemBytes, stream>>>(a, qmap);
     e = cudaGetLastError();
     if (e != cudaSuccess || plan.nsplit == 1) return e;
-    combine_kernel<<<B * H, 128, 0, stream>>>(part_o, part_lse, plan.nsplit, H, o, lse);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(B * H);
+    cfg.blockDim = dim3(128);
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, combine_kernel, (const float*)part_o, (const float*)part_lse, plan.nsplit, H, o, lse);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
