@@ -10,15 +10,21 @@
 // R^576, value V_j = latent_j in R^512, per head s_hj = sm_scale * <q_h, K_j> over the
 // selections whose slot is valid, o_h = softmax(s_h) V, lse_h = ln sum_j exp(s_hj).
 //
-// attend_kernel: one CTA per (request b, key split s, value half v), 800 threads, one CTA
+// attend_kernel: one CTA per (request b, key split s, value half v), 832 threads, one CTA
 // per SM (209 KB of shared memory, 512 TMEM columns).
-//   * Keys come in blocks of 256 selections. 16 producer warps gather their rows through
-//     out_slots, decode the E4M3 codes times their block scale to bf16 and fill a ring of
-//     four 48 KB stages: per block nine K fills (256 keys x 64 dims, K-major) and four V
-//     fills (64 keys x this CTA's 256 value dims, read MN-major).
+//   * Keys come in blocks of 256 selections, and the stages of a ring of four 48 KB
+//     stages are filled in the order the MMAs consume them: per block nine K fills (256
+//     keys x 64 dims, K-major; 8 latent chunks, then the rotary one) and four V fills (64
+//     keys x this CTA's 256 value dims, read MN-major). A fill gathers its rows through
+//     out_slots and decodes the E4M3 codes times their block scale to bf16 (the rotary
+//     values are bf16 already and are copied as they are). 16 producer warps make six of
+//     the K fills and the V fills; the 8 softmax warps, idle while a block's scores are
+//     being multiplied, make the other three K fills of the block (latent chunks 2 and 5
+//     and the rotary chunk) before they wait for its scores.
 //   * Q [H x 576] bf16 is not kept resident: a K fill's stage also receives the matching
 //     64-dimension column of Q (128 rows x 128 bytes) by one tensor-memory-access copy
-//     (TMA, 128-byte swizzle, rows beyond H zero-filled) that lands on its own mbarrier.
+//     (TMA, 128-byte swizzle, rows beyond H zero-filled) that lands on its own mbarrier;
+//     one thread of its own warp issues these copies as soon as each stage is free.
 //     Freeing Q's 147 KB of shared memory is what pays for the four-deep ring, so the
 //     producers keep filling while the softmax runs.
 //   * one thread issues the MMAs: S = Q K^T (M=128 heads, N=256 keys, K=16 per
@@ -41,7 +47,7 @@
 // Every wait on an mbarrier is bounded in time (global timer, the context's wait limit
 // counted from the CTA's start): on expiry the CTA records HS_STATUS_TIMEOUT, every role
 // leaves its loop, the MMA thread waits (again bounded in time) for its own MMAs and the
-// producers for their last Q copies, and the TMEM columns are freed before the CTA exits.
+// Q thread for its last copies, and the TMEM columns are freed before the CTA exits.
 #include <cuda.h>  // CUtensorMap (the encoder is reached through the runtime's entry point)
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -69,19 +75,34 @@ constexpr int kVFills = kBlk / kVKeys;               // V chunks per block
 constexpr int kFills = kKFills + kVFills;            // stage fills per block
 constexpr uint32_t kVSub = kVKeys * 128;             // bytes of one 64-dimension column of a V chunk
 constexpr int kSoftWarps = 8, kProdWarps = 16;  // softmax: two groups of 4 warps, 128 keys each
-constexpr int kThreads = (kSoftWarps + kProdWarps + 1) * 32;  // 800
-constexpr int kMmaWarp = kSoftWarps + kProdWarps;
+constexpr int kMmaWarp = kSoftWarps + kProdWarps;  // then one warp for the Q copies
+constexpr int kQWarp = kMmaWarp + 1;
+constexpr int kThreads = (kQWarp + 1) * 32;  // 832
+// The softmax warps, idle while a block's scores are being multiplied, fill three of its
+// nine K chunks (latent chunks 2 and 5 and the rotary chunk); the producers fill the
+// other six and the four V chunks.
+constexpr int kProdFills = 10;  // producer fills per block: 0, 1, 3, 4, 6, 7, then V 9..12
+__host__ __device__ constexpr int prod_fill(int j) { return j + (j >= 2) + (j >= 4) + (j >= 6); }
+constexpr bool fills_split_once() {  // the two lists cover a block's 13 fills, each once
+    int seen = (1 << 2) | (1 << 5) | (1 << 8);
+    for (int j = 0; j < kProdFills; ++j) {
+        if ((seen >> prod_fill(j)) & 1) return false;
+        seen |= 1 << prod_fill(j);
+    }
+    return seen == (1 << kFills) - 1;
+}
+static_assert(fills_split_once(), "fills of a block");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256;  // O: 256 columns; S: 256 columns, P (bf16) written over its first 128
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kMaxSplitKeys = 2048;        // slots of one split staged in shared memory
 
 // barrier indices
-enum { kFull = 0 /* kStages: producers' fills */, kFree = 4 /* kStages: MMAs done with a stage */,
-       kQLand = 8 /* kStages: a stage's Q chunk has landed */, kSFull = 12, kPvDone = 13,
-       kVmFull = 14 /* 2, by block parity */, kDrain = 16, kBmax = 17 /* 2, by block parity */, kLsum = 19,
-       kPHalf = 20 /* 4: [softmax group][first or second half of its keys]: P written */, kBars = 24 };
-static_assert(kFree == kFull + kStages && kQLand == kFree + kStages && kSFull == kQLand + kStages, "barrier map");
+enum { kFull = 0 /* kStages: a stage's fill is written */, kFree = 4 /* 2 kStages: MMAs done with fill g, by g % 8 */,
+       kQLand = 12 /* kStages: a stage's Q chunk has landed */, kSFull = 16, kPvDone = 17,
+       kVmFull = 18 /* 2, by block parity */, kDrain = 20, kBmax = 21 /* 2, by block parity */, kLsum = 23,
+       kPHalf = 24 /* 4: [softmax group][first or second half of its keys]: P written */, kBars = 28 };
+static_assert(kFree == kFull + kStages && kQLand == kFree + 2 * kStages && kSFull == kQLand + kStages, "barrier map");
 
 struct Smem {  // beyond Q and the stages
     int32_t slot[kMaxSplitKeys];  // this split's out_slots
@@ -114,6 +135,9 @@ __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvt
 // ---------------------------------------------------------------- mbarriers
 __device__ __forceinline__ void bar_init(uint64_t* b, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void bar_arrive2(uint64_t* b) {  // counts as two arrivals
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0], 2; }" ::"r"(su32(b)) : "memory");
 }
 __device__ __forceinline__ void bar_arrive(uint64_t* b) {
     asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(su32(b)) : "memory");
@@ -150,6 +174,19 @@ __device__ __forceinline__ bool warp_wait(Smem* sm, uint64_t* b, uint32_t parity
 __device__ __forceinline__ void drain_wait(uint64_t* b, uint32_t parity, uint64_t deadline) {
     while (!bar_try(b, parity) && global_ns() <= deadline) {
     }
+}
+
+// The wait of a writer of fill g (of any role): the previous fill of its stage, g - 4, has
+// been consumed. The MMA thread signals the consumption of fill g on barrier g % 8 -- two
+// barriers per stage, used alternately -- so that a parity wait stays unambiguous for a
+// writer whose previous write (or wait) was up to 8 fills earlier: the producers' fills
+// are at most 3 apart, the softmax warps' 7 (from a block's rotary chunk to the next
+// block's chunk 2), the Q thread's 5. With one barrier per stage, a writer returning after
+// two phases of the stage could not tell them apart.
+__device__ __forceinline__ bool wait_free(Smem* sm, int g, uint32_t* status, uint64_t deadline) {
+    if (g < kStages) return true;
+    const int p = g - kStages;
+    return bar_wait(sm, &sm->bar[kFree + p % (2 * kStages)], (p / (2 * kStages)) & 1, status, deadline);
 }
 
 // ---------------------------------------------------------------- TMA
@@ -252,6 +289,77 @@ __device__ __forceinline__ uint4 decode8(uint32_t lo, uint32_t hi, float scale) 
 // Byte offset of 16-byte unit u (0..7) of row r in a 128-byte-swizzled column chunk.
 __device__ __forceinline__ uint32_t swz(int r, int u) { return (uint32_t)(r * 128 + ((u ^ (r & 7)) << 4)); }
 
+// ---------------------------------------------------------------- stage fills
+// A CTA's keys: request b's device rows and the split's slots, staged in shared memory.
+struct Keys {
+    const uint8_t* dev;
+    int S, b, kbeg, kend;
+    const int32_t* slot;
+    __device__ __forceinline__ int32_t at(int j) const {  // key j of the split; -1 when past its end or invalid
+        const int32_t s = kbeg + j < kend ? slot[j] : -1;
+        return (s >= 0 && s < S) ? s : -1;
+    }
+    __device__ __forceinline__ const uint8_t* row(int32_t s) const { return dev + ((size_t)b * S + s) * 656; }
+};
+// The raw bytes one of NT threads decodes into a K chunk (256 keys x 64 dims): groups of
+// 16 codes with their block scale. Thread t's keys are (t >> 2) + (NT / 4) w, its codes
+// those of dimensions 64 f + 16 (t & 3) ... + 15: the 4 lanes of a key read 64 whole bytes.
+template <int NT>
+struct RawK {
+    static constexpr int kItems = 1024 / NT;
+    uint4 c[kItems];
+    float scale[kItems];
+};
+template <int NT>
+__device__ __forceinline__ void k_rows(const Keys& K, int t, int i, const uint8_t* (&rows)[1024 / NT]) {
+#pragma unroll
+    for (int w = 0; w < 1024 / NT; ++w) {
+        const int32_t s = K.at(i * kBlk + (t >> 2) + (NT / 4) * w);
+        rows[w] = s >= 0 ? K.row(s) : nullptr;  // nullptr: no key, zeros
+    }
+}
+template <int NT>
+__device__ __forceinline__ void k_load(const uint8_t* const (&rows)[1024 / NT], int t, int f, RawK<NT>& r) {
+    const int off = 64 * f + 16 * (t & 3);
+#pragma unroll
+    for (int w = 0; w < RawK<NT>::kItems; ++w) {
+        if (rows[w]) {
+            r.c[w] = __ldg(reinterpret_cast<const uint4*>(rows[w] + off));
+            r.scale[w] = __ldg(reinterpret_cast<const float*>(rows[w] + 512) + (off >> 7));
+        } else {
+            r.c[w] = make_uint4(0, 0, 0, 0);
+            r.scale[w] = 0.f;
+        }
+    }
+}
+template <int NT>
+__device__ __forceinline__ void k_store(uint8_t* stg, int t, const RawK<NT>& r) {
+    const int q = t & 3;
+#pragma unroll
+    for (int w = 0; w < RawK<NT>::kItems; ++w) {
+        const int key = (t >> 2) + (NT / 4) * w;
+        *reinterpret_cast<uint4*>(stg + swz(key, 2 * q)) = decode8(r.c[w].x, r.c[w].y, r.scale[w]);
+        *reinterpret_cast<uint4*>(stg + swz(key, 2 * q + 1)) = decode8(r.c[w].z, r.c[w].w, r.scale[w]);
+    }
+}
+// The rotary chunk of block i (256 keys x 64 bf16, copied as it is) by NT threads with
+// asynchronous 16-byte copies, 8 lanes per key; missing keys read as zero. Returns once
+// the copies have landed.
+template <int NT>
+__device__ __forceinline__ void rope_copy(const Keys& K, uint8_t* stg, int t, int i) {
+    const int u = t & 7;
+#pragma unroll
+    for (int w = 0; w < 2048 / NT; ++w) {
+        const int key = (t >> 3) + (NT / 8) * w;
+        const int32_t s = K.at(i * kBlk + key);
+        const uint8_t* src = K.row(s >= 0 ? s : 0) + 528 + 16 * u;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(su32(stg + swz(key, u))), "l"(src),
+                     "r"(s >= 0 ? 16u : 0u) : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A, const __grid_constant__ CUtensorMap qmap) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -271,6 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
         for (int st = 0; st < kStages; ++st) {
             bar_init(&sm->bar[kFull + st], kProdWarps * 32);
             bar_init(&sm->bar[kFree + st], 1);
+            bar_init(&sm->bar[kFree + kStages + st], 1);
             bar_init(&sm->bar[kQLand + st], 1);
         }
         bar_init(&sm->bar[kVmFull], kBlk / 32);
@@ -298,69 +407,49 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
     if (warp >= kSoftWarps && warp < kMmaWarp) {
         // ------------------------------------------------------------ producers
         const int pw = warp - kSoftWarps;
-        const int ptid = tid - kSoftWarps * 32;  // 0..255
-        // the split's slots, staged once
+        const int ptid = tid - kSoftWarps * 32;  // 0..511
+        // the split's slots, staged once for the producers and the softmax warps
         const int32_t* slots = A.out_slots + (size_t)b * A.k;
         for (int j = ptid; j < kend - kbeg; j += kProdWarps * 32) sm->slot[j] = __ldg(slots + kbeg + j);
-        asm volatile("bar.sync 1, %0;" ::"r"(kProdWarps * 32) : "memory");
-        auto slot_at = [&](int j) -> int32_t {  // key j of the split; -1 when past its end or invalid
-            const int32_t s = kbeg + j < kend ? sm->slot[j] : -1;
-            return (s >= 0 && s < A.S) ? s : -1;
-        };
-        auto row_of = [&](int32_t s) { return A.dev + ((size_t)b * A.S + s) * 656; };
+        asm volatile("bar.sync 1, %0;" ::"r"((kProdWarps + kSoftWarps) * 32) : "memory");
+        const Keys K{A.dev, A.S, b, kbeg, kend, sm->slot};
         auto prefetch_block = [&](int i) {  // this warp's 32 rows of the block into L2
             if (i >= nb || ptid >= kBlk) return;
-            const int32_t s = slot_at(i * kBlk + ptid);
-            if (s >= 0) asm volatile("cp.async.bulk.prefetch.L2.global [%0], 656;" ::"l"(row_of(s)) : "memory");
+            const int32_t s = K.at(i * kBlk + ptid);
+            if (s >= 0) asm volatile("cp.async.bulk.prefetch.L2.global [%0], 656;" ::"l"(K.row(s)) : "memory");
         };
         prefetch_block(0);
-        // Stage fills, in the order the MMAs consume them: per block the 9 K chunks (8
-        // latent, then the rotary one) and the 4 V chunks. Loads are spread so that the
-        // lanes of a warp read a few whole stretches of a row each (4 lanes x 16 bytes
-        // per key for a K chunk, 16 lanes for a V chunk, 8 lanes for the rotary chunk):
-        // a warp-wide load then touches 8 (or 2, or 4) rows rather than 32. The raw bytes
-        // of fill g + 2 are requested before fill g is decoded; three register buffers
-        // rotate by unrolling, so two fills' loads are always in flight.
-        constexpr int kW = 1024 / (kProdWarps * 32);  // (key, 16-byte unit) items per thread in a K or V chunk
-        struct Raw {
-            uint4 c[kW];
-            float scale[kW];
-        };
-        const int total = nb * kFills;
-        uint32_t qpar = 0, qout = 0;  // (thread 0) per stage: phase parity of its next Q copy; copies issued
-        const int kq = ptid & 3, kkey = ptid >> 2;    // K chunk: quarter of the 64 dims, key (+128 w)
-        const int vu = ptid & 15, vkey = ptid >> 4;   // V chunk: 16-dim unit of the half, key (+32 w)
-        const int rq = ptid & 7, rkey = ptid >> 3;    // rotary chunk: 16-byte unit, key (+64 w)
-        // This thread's K rows are the same for the eight latent fills of a block: they are
+        // The producers' fills, in the order the MMAs consume them: per block six of the
+        // K chunks (the softmax warps fill the other three) and the 4 V chunks. Loads are
+        // spread so that the lanes of a warp read a few whole stretches of a row each (4
+        // lanes x 16 bytes per key for a K chunk, 16 lanes for a V chunk): a warp-wide
+        // load then touches 8 (or 2) rows rather than 32. The raw bytes of fill j + 2 are
+        // requested before fill j is decoded; three register buffers rotate by unrolling,
+        // so two fills' loads are always in flight.
+        const int total = nb * kProdFills;
+        const int vu = ptid & 15, vkey = ptid >> 4;  // V chunk: 16-dim unit of the half, key (+32 w)
+        // This thread's K rows are the same for the latent fills of a block: they are
         // looked up once per block (a shared-memory read before every load would queue
         // behind the stage stores and delay the loads' issue).
-        const uint8_t* krow[kW];
+        const uint8_t* krow[RawK<kProdWarps * 32>::kItems];
         int kblock = -1;
-        auto issue = [&](int g, Raw& r) {
-            if (g >= total) return;
-            const int i = g / kFills, f = g - i * kFills;
-            if (f == kKFills - 1) return;  // the rotary chunk is copied asynchronously
-            if (f < kKFills && i != kblock) {
-#pragma unroll
-                for (int w = 0; w < kW; ++w) {
-                    const int32_t s = slot_at(i * kBlk + kkey + 128 * w);
-                    krow[w] = s >= 0 ? row_of(s) : nullptr;
+        auto issue = [&](int j, RawK<kProdWarps * 32>& r) {
+            if (j >= total) return;
+            const int i = j / kProdFills, f = prod_fill(j - i * kProdFills);
+            if (f < kKFills) {
+                if (i != kblock) {
+                    k_rows<kProdWarps * 32>(K, ptid, i, krow);
+                    kblock = i;
                 }
-                kblock = i;
+                k_load<kProdWarps * 32>(krow, ptid, f, r);
+                return;
             }
 #pragma unroll
-            for (int w = 0; w < kW; ++w) {
-                const uint8_t* row;
-                int off;
-                if (f < kKFills) {
-                    row = krow[w];
-                    off = 64 * f + 16 * kq;
-                } else {
-                    const int32_t s = slot_at(i * kBlk + (f - kKFills) * kVKeys + vkey + 32 * w);
-                    row = s >= 0 ? row_of(s) : nullptr;
-                    off = kHalfV * v + 16 * vu;
-                }
-                if (row) {
+            for (int w = 0; w < RawK<kProdWarps * 32>::kItems; ++w) {
+                const int32_t s = K.at(i * kBlk + (f - kKFills) * kVKeys + vkey + 32 * w);
+                const int off = kHalfV * v + 16 * vu;
+                if (s >= 0) {
+                    const uint8_t* row = K.row(s);
                     r.c[w] = __ldg(reinterpret_cast<const uint4*>(row + off));
                     r.scale[w] = __ldg(reinterpret_cast<const float*>(row + 512) + (off >> 7));
                 } else {
@@ -369,48 +458,26 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
                 }
             }
         };
-        auto process = [&](int g, const Raw& r) -> bool {
-            const int i = g / kFills, f = g - i * kFills;
-            if (f == 0 && pw < kBlk / 32) {  // a new block: its valid keys (32 per warp)
-                const uint32_t m = __ballot_sync(0xffffffffu, slot_at(i * kBlk + ptid) >= 0);
+        auto process = [&](int j, const RawK<kProdWarps * 32>& r) -> bool {
+            const int i = j / kProdFills, jj = j - i * kProdFills, f = prod_fill(jj);
+            const int g = i * kFills + f;
+            if (jj == 0 && pw < kBlk / 32) {  // a new block: its valid keys (32 per warp)
+                const uint32_t m = __ballot_sync(0xffffffffu, K.at(i * kBlk + ptid) >= 0);
                 if (lane == 0) {
                     sm->vmask[i & 1][pw] = m;
                     bar_arrive(&sm->bar[kVmFull + (i & 1)]);
                 }
             }
-            if (pw < kBlk / 32 && f == pw) prefetch_block(i + 1);  // the next block's rows into L2
+            if (pw < kBlk / 32 && jj == pw) prefetch_block(i + 1);  // the next block's rows into L2
             const int st = g % kStages;
-            if (g >= kStages && !bar_wait(sm, &sm->bar[kFree + st], ((g / kStages) & 1) ^ 1, A.status, deadline)) return false;
-            uint8_t* slot = ring + st * kSlotBytes;
-            if (f < kKFills && ptid == 0) {  // the matching 64-dimension column of Q, by one TMA copy
-                bar_expect_tx(&sm->bar[kQLand + st], kQChunk);
-                tma_load_q(slot, &qmap, 64 * f, b, &sm->bar[kQLand + st]);
-                qpar ^= 1u << st;
-                qout |= 1u << st;
-            }
-            uint8_t* stg = slot + kQChunk;
-            if (f == kKFills - 1) {  // rotary values: bf16 already, copied as they are
-#pragma unroll
-                for (int w = 0; w < 2 * kW; ++w) {
-                    const int key = rkey + 64 * w;
-                    const int32_t s = slot_at(i * kBlk + key);
-                    const uint8_t* src = row_of(s >= 0 ? s : 0) + 528 + 16 * rq;
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(su32(stg + swz(key, rq))),
-                                 "l"(src), "r"(s >= 0 ? 16u : 0u) : "memory");
-                }
-                asm volatile("cp.async.commit_group;" ::: "memory");
-                asm volatile("cp.async.wait_all;" ::: "memory");
-            } else if (f < kKFills) {
-#pragma unroll
-                for (int w = 0; w < kW; ++w) {
-                    const int key = kkey + 128 * w;
-                    *reinterpret_cast<uint4*>(stg + swz(key, 2 * kq)) = decode8(r.c[w].x, r.c[w].y, r.scale[w]);
-                    *reinterpret_cast<uint4*>(stg + swz(key, 2 * kq + 1)) = decode8(r.c[w].z, r.c[w].w, r.scale[w]);
-                }
+            if (!wait_free(sm, g, A.status, deadline)) return false;
+            uint8_t* stg = ring + st * kSlotBytes + kQChunk;
+            if (f < kKFills) {
+                k_store<kProdWarps * 32>(stg, ptid, r);
             } else {
                 uint8_t* col = stg + (vu >> 2) * kVSub;  // the 64-dim column of this unit
 #pragma unroll
-                for (int w = 0; w < kW; ++w) {
+                for (int w = 0; w < RawK<kProdWarps * 32>::kItems; ++w) {
                     const int key = vkey + 32 * w;
                     *reinterpret_cast<uint4*>(col + swz(key, 2 * (vu & 3))) = decode8(r.c[w].x, r.c[w].y, r.scale[w]);
                     *reinterpret_cast<uint4*>(col + swz(key, 2 * (vu & 3) + 1)) = decode8(r.c[w].z, r.c[w].w, r.scale[w]);
@@ -420,24 +487,16 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
             if (!(A.stall && g == 0)) bar_arrive(&sm->bar[kFull + st]);
             return true;
         };
-        Raw r0, r1, r2;
+        RawK<kProdWarps * 32> r0, r1, r2;
         issue(0, r0);
         issue(1, r1);
-        for (int g = 0; g < total; g += 3) {
-            issue(g + 2, r2);
-            if (!process(g, r0) || g + 1 >= total) break;
-            issue(g + 3, r0);
-            if (!process(g + 1, r1) || g + 2 >= total) break;
-            issue(g + 4, r1);
-            if (!process(g + 2, r2)) break;
-        }
-        // No Q copy may still be landing when the CTA exits (after an abort the MMA thread
-        // may not have waited for the last ones): wait, bounded, for the last copy issued
-        // into each stage.
-        if (ptid == 0) {
-            const uint64_t drain_by = global_ns() + A.wait_ns;
-            for (int st = 0; st < kStages; ++st)
-                if ((qout >> st) & 1u) drain_wait(&sm->bar[kQLand + st], ((qpar >> st) & 1u) ^ 1u, drain_by);
+        for (int j = 0; j < total; j += 3) {
+            issue(j + 2, r2);
+            if (!process(j, r0) || j + 1 >= total) break;
+            issue(j + 3, r0);
+            if (!process(j + 1, r1) || j + 2 >= total) break;
+            issue(j + 4, r1);
+            if (!process(j + 2, r2)) break;
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issue (one thread)
@@ -461,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
                     for (int kk = 0; kk < 4; ++kk)
                         mma_ss(tmem + kColS, smem_desc(qa + kk * 32, 16, 1024), smem_desc(kb + kk * 32, 16, 1024),
                                id_s, (c | kk) ? 1u : 0u);
-                    mma_commit(&sm->bar[kFree + st]);
+                    mma_commit(&sm->bar[kFree + g % (2 * kStages)]);
                 }
                 if (!ok) break;
                 mma_commit(&sm->bar[kSFull]);
@@ -479,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
                     for (int ks = 0; ks < kVKeys / 16; ++ks)
                         mma_ts(tmem + kColO, tmem + kColS + (kVKeys / 2) * vc + 8 * ks + (vc >= kVFills / 2 ? 64 : 0),
                                smem_desc(vb + ks * 2048, kVSub, 1024), id_o, (i > 0 || j > 0 || ks > 0) ? 1u : 0u);
-                    mma_commit(&sm->bar[kFree + st]);
+                    mma_commit(&sm->bar[kFree + gv % (2 * kStages)]);
                 }
                 g += kVFills;
                 if (!ok) break;
@@ -488,6 +547,30 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
             // whatever happened, every MMA issued here completes before the columns are freed
             mma_commit(&sm->bar[kDrain]);
             drain_wait(&sm->bar[kDrain], 0, global_ns() + A.wait_ns);
+        }
+        __syncwarp();
+    } else if (warp == kQWarp) {
+        // ------------------------------------------------------------ Q copies (one thread)
+        // Each K fill's stage also receives the matching 64-dimension column of Q, by one TMA
+        // copy issued as soon as the stage is free.
+        if (lane == 0) {
+            uint32_t qpar = 0, qout = 0;  // per stage: phase parity of its next Q copy; copies issued
+            const int total = nb * kFills;
+            for (int g = 0; g < total; ++g) {
+                const int f = g % kFills, st = g % kStages;
+                if (f >= kKFills) continue;
+                if (!wait_free(sm, g, A.status, deadline)) break;
+                bar_expect_tx(&sm->bar[kQLand + st], kQChunk);
+                tma_load_q(ring + st * kSlotBytes, &qmap, 64 * f, b, &sm->bar[kQLand + st]);
+                qpar ^= 1u << st;
+                qout |= 1u << st;
+            }
+            // No Q copy may still be landing when the CTA exits (after an abort the MMA thread
+            // may not have waited for the last ones): wait, bounded, for the last copy issued
+            // into each stage.
+            const uint64_t drain_by = global_ns() + A.wait_ns;
+            for (int st = 0; st < kStages; ++st)
+                if ((qout >> st) & 1u) drain_wait(&sm->bar[kQLand + st], ((qpar >> st) & 1u) ^ 1u, drain_by);
         }
         __syncwarp();
     } else {
@@ -502,7 +585,39 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
         const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lanes
         float m = -INFINITY, l = 0.f;
         bool ok = true;
+        asm volatile("bar.sync 1, %0;" ::"r"((kProdWarps + kSoftWarps) * 32) : "memory");  // slots staged
+        const Keys K{A.dev, A.S, b, kbeg, kend, sm->slot};
+        // Fill g's stage, once free (nullptr once the CTA has aborted); the caller stores into
+        // it and calls close_fill.
+        auto open_fill = [&](int g) -> uint8_t* {
+            const int st = g % kStages;
+            if (!__all_sync(0xffffffffu, wait_free(sm, g, A.status, deadline))) return nullptr;
+            return ring + st * kSlotBytes + kQChunk;
+        };
+        auto close_fill = [&](int g) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            bar_arrive2(&sm->bar[kFull + g % kStages]);  // 256 threads stand for the producers' 512
+        };
         for (int i = 0; i < nb; ++i) {
+            {  // while the producers fill the rest of the block: its K chunks 2 and 5 and the rotary one
+                constexpr int NT = kSoftWarps * 32;
+                const uint8_t* hrow[RawK<NT>::kItems];
+                k_rows<NT>(K, tid, i, hrow);
+                RawK<NT> h0, h1;
+                k_load<NT>(hrow, tid, 2, h0);
+                k_load<NT>(hrow, tid, 5, h1);
+                const int g0 = i * kFills;
+                uint8_t* stg = open_fill(g0 + 2);
+                if (!stg) { ok = false; break; }
+                k_store<NT>(stg, tid, h0);
+                close_fill(g0 + 2);
+                if (!(stg = open_fill(g0 + 5))) { ok = false; break; }
+                k_store<NT>(stg, tid, h1);
+                close_fill(g0 + 5);
+                if (!(stg = open_fill(g0 + kKFills - 1))) { ok = false; break; }
+                rope_copy<NT>(K, stg, tid, i);
+                close_fill(g0 + kKFills - 1);
+            }
             if (!warp_wait(sm, &sm->bar[kSFull], i & 1, A.status, deadline) ||
                 !warp_wait(sm, &sm->bar[kVmFull + (i & 1)], (i >> 1) & 1, A.status, deadline)) { ok = false; break; }
             fence_after();
