@@ -629,9 +629,19 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
                 HS_LD32(r, tmem + lrow + kColS + 32 * ch);
                 tmem_wait_ld();
                 const uint32_t vm = sm->vmask[i & 1][ch];
+                if (vm == 0xffffffffu && A.scale_log2 > 0.f) {
+                    // every key valid: the largest score, scaled once (a positive scale keeps
+                    // the order of the rounded products, so the result is the same)
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if ((vm >> j) & 1u) mb = fmaxf(mb, __uint_as_float(r[j]) * A.scale_log2);
+                    for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+                        for (int j = 0; j < w; ++j) r[j] = __float_as_uint(fmaxf(__uint_as_float(r[j]), __uint_as_float(r[j + w])));
+                    mb = fmaxf(mb, __uint_as_float(r[0]) * A.scale_log2);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if ((vm >> j) & 1u) mb = fmaxf(mb, __uint_as_float(r[j]) * A.scale_log2);
+                }
             }
             sm->bmax[i & 1][grp][h] = mb;
             bar_arrive(&sm->bar[kBmax + (i & 1)]);
@@ -666,14 +676,26 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
                 tmem_wait_ld();
                 const uint32_t vm = sm->vmask[i & 1][ch];
                 uint32_t pk[16];
+                if (vm == 0xffffffffu) {  // every key valid
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float p0 = ((vm >> (2 * c)) & 1u) ? ex2(__uint_as_float(r[2 * c]) * A.scale_log2 - m) : 0.f;
-                    const float p1 = ((vm >> (2 * c + 1)) & 1u) ? ex2(__uint_as_float(r[2 * c + 1]) * A.scale_log2 - m) : 0.f;
-                    const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-                    const float2 pr = __bfloat1622float2(pb);
-                    l += pr.x + pr.y;
-                    pk[c] = *reinterpret_cast<const uint32_t*>(&pb);
+                    for (int c = 0; c < 16; ++c) {
+                        const float p0 = ex2(__uint_as_float(r[2 * c]) * A.scale_log2 - m);
+                        const float p1 = ex2(__uint_as_float(r[2 * c + 1]) * A.scale_log2 - m);
+                        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+                        const float2 pr = __bfloat1622float2(pb);
+                        l += pr.x + pr.y;
+                        pk[c] = *reinterpret_cast<const uint32_t*>(&pb);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const float p0 = ((vm >> (2 * c)) & 1u) ? ex2(__uint_as_float(r[2 * c]) * A.scale_log2 - m) : 0.f;
+                        const float p1 = ((vm >> (2 * c + 1)) & 1u) ? ex2(__uint_as_float(r[2 * c + 1]) * A.scale_log2 - m) : 0.f;
+                        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+                        const float2 pr = __bfloat1622float2(pb);
+                        l += pr.x + pr.y;
+                        pk[c] = *reinterpret_cast<const uint32_t*>(&pb);
+                    }
                 }
                 HS_ST16(tmem + lrow + kColS + 16 * ch + 64 * grp, pk);
                 if (ch & 1) {  // 64 keys written: their part of P V may start
