@@ -81,17 +81,25 @@ constexpr int kThreads = (kQWarp + 1) * 32;  // 832
 // The softmax warps, idle while a block's scores are being multiplied, fill three of its
 // nine K chunks (latent chunks 2 and 5 and the rotary chunk); the producers fill the
 // other six and the four V chunks.
-constexpr int kProdFills = 10;  // producer fills per block: 0, 1, 3, 4, 6, 7, then V 9..12
-__host__ __device__ constexpr int prod_fill(int j) { return j + (j >= 2) + (j >= 4) + (j >= 6); }
+constexpr int kHelp0 = 2, kHelp1 = 5, kHelp2 = 8;  // the softmax warps' K fills of a block, in order
+constexpr int kProdFills = kFills - 3;    // the producers': the other six K fills, then V 9..12
+__host__ __device__ constexpr int prod_fill(int j) {  // the producers' j-th fill of a block
+    return j + (j >= kHelp0) + (j + 1 >= kHelp1) + (j + 2 >= kHelp2);
+}
 constexpr bool fills_split_once() {  // the two lists cover a block's 13 fills, each once
-    int seen = (1 << 2) | (1 << 5) | (1 << 8);
+    int seen = (1 << kHelp0) | (1 << kHelp1) | (1 << kHelp2);
     for (int j = 0; j < kProdFills; ++j) {
         if ((seen >> prod_fill(j)) & 1) return false;
         seen |= 1 << prod_fill(j);
     }
-    return seen == (1 << kFills) - 1;
+    return seen == (1 << kFills) - 1 && kHelp2 == kKFills - 1;  // the last is the rotary chunk
 }
 static_assert(fills_split_once(), "fills of a block");
+// Every writer's fills are at most 2 kStages apart, the window in which the parity waits on
+// the free barriers stay unambiguous (see wait_free).
+static_assert(kFills + kHelp0 - kHelp2 <= 2 * kStages && kHelp1 - kHelp0 <= 2 * kStages &&
+                  kHelp2 - kHelp1 <= 2 * kStages,
+              "the softmax warps' fills must stay within the free barriers' window");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256;  // O: 256 columns; S: 256 columns, P (bf16) written over its first 128
 constexpr float kRescaleLog2 = 8.0f;
@@ -604,16 +612,16 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
                 const uint8_t* hrow[RawK<NT>::kItems];
                 k_rows<NT>(K, tid, i, hrow);
                 RawK<NT> h0, h1;
-                k_load<NT>(hrow, tid, 2, h0);
-                k_load<NT>(hrow, tid, 5, h1);
+                k_load<NT>(hrow, tid, kHelp0, h0);
+                k_load<NT>(hrow, tid, kHelp1, h1);
                 const int g0 = i * kFills;
-                uint8_t* stg = open_fill(g0 + 2);
+                uint8_t* stg = open_fill(g0 + kHelp0);
                 if (!stg) { ok = false; break; }
                 k_store<NT>(stg, tid, h0);
-                close_fill(g0 + 2);
-                if (!(stg = open_fill(g0 + 5))) { ok = false; break; }
+                close_fill(g0 + kHelp0);
+                if (!(stg = open_fill(g0 + kHelp1))) { ok = false; break; }
                 k_store<NT>(stg, tid, h1);
-                close_fill(g0 + 5);
+                close_fill(g0 + kHelp1);
                 if (!(stg = open_fill(g0 + kKFills - 1))) { ok = false; break; }
                 rope_copy<NT>(K, stg, tid, i);
                 close_fill(g0 + kKFills - 1);
