@@ -213,6 +213,27 @@ def test_attend_all_padding_and_permutation():
     ctx.close()
 
 
+def test_attend_negative_scale():
+    """A negative softmax scale: the block maximum is then taken over the scaled scores key
+    by key (the raw maximum is the scaled minimum), with and without padding."""
+    rows = [gaussian_rows(300, 7), gaussian_rows(40, 8)]
+    ctx, orc, out, o_out = _context_with_rows(rows, S=320)
+    out_np = out.cpu().numpy()
+    out_np[1, 33:] = -1
+    o_out[1, 33:] = -1
+    rng = np.random.default_rng(9)
+    q = bf16_tensor(rng.standard_normal((2, 64, 576)))
+    sm = -1.0 / math.sqrt(576)
+    o_gpu, lse_gpu = run_attend(ctx, q.cuda(), torch.from_numpy(out_np).cuda(), sm)
+    qb = q.view(torch.int16).numpy().view(np.uint16)
+    dev = ctx.device_kv().cpu().numpy()
+    for b in range(2):
+        o_ref, lse_ref, absw = orc.attend(b, qb[b], o_out[b], sm)
+        ds = score_rounding(dev[b], o_out[b], qb[b], abs(sm))
+        compare(o_gpu[b], lse_gpu[b], o_ref, lse_ref, absw, f"negative scale, request {b}", ds)
+    ctx.close()
+
+
 def test_attend_full_size_dsa_sampled():
     """32 requests x k = 2048 x 128 heads (the DSA workload), three requests checked."""
     w = tracegen.WORKLOADS["dsa"]
