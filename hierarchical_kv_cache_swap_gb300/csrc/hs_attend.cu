@@ -40,9 +40,10 @@
 //     as soon as their P is written, and the product over those keys starts then, so
 //     the P V MMAs run under the rest of the softmax.
 // With several key splits per request each CTA writes its normalised partial and its
-// lse; combine_kernel merges them (weights exp(lse_s - lse)). It is launched as a
-// programmatic dependent of attend_kernel, so its launch overlaps the attention and
-// its blocks wait (griddepcontrol.wait) only for the attention's results.
+// lse; combine_kernel merges them (weights exp(lse_s - lse)). It is an ordinary launch:
+// as a programmatic dependent started at the attention's beginning, its waiting blocks
+// took the SMs the attention leaves free, which another stream's work (the next layer's
+// resolution) needs.
 //
 // Every wait on an mbarrier is bounded in time (global timer, the context's wait limit
 // counted from the CTA's start): on expiry the CTA records HS_STATUS_TIMEOUT, every role
@@ -381,7 +382,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
     const int kend = min(A.k, kbeg + A.keys_per_split);
     const int nb = kend > kbeg ? (kend - kbeg + kBlk - 1) / kBlk : 0;
     const uint64_t deadline = global_ns() + A.wait_ns;  // every wait of this CTA ends by then
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (tid == 0) {
         for (int st = 0; st < kStages; ++st) {
@@ -765,7 +765,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttendArgs A,
 __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                                                       int nsplit, int H, float* __restrict__ o, float* __restrict__ lse) {
     const int bh = blockIdx.x, b = bh / H, h = bh - b * H;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     float mx = -INFINITY;
     for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, part_lse[((size_t)b * nsplit + s) * H + h]);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -883,17 +882,7 @@ cudaError_t launch_attend(const Layout& L, cudaStream_t stream, const uint16_t* 
     attend_kernel<<<B * plan.nsplit * 2, kThreads, kSmemBytes, stream>>>(a, qmap);
     e = cudaGetLastError();
     if (e != cudaSuccess || plan.nsplit == 1) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(B * H);
-    cfg.blockDim = dim3(128);
-    cfg.stream = stream;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, combine_kernel, (const float*)part_o, (const float*)part_lse, plan.nsplit, H, o, lse);
-    if (e != cudaSuccess) return e;
+    combine_kernel<<<B * H, 128, 0, stream>>>(part_o, part_lse, plan.nsplit, H, o, lse);
     return cudaGetLastError();
 }
 
