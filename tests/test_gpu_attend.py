@@ -234,6 +234,37 @@ def test_attend_negative_scale():
     ctx.close()
 
 
+def test_attend_random_shapes():
+    """Seeded random shapes: ragged last blocks, one to several key splits, any head count
+    and padding scattered through the selections, so that every fill role (producers,
+    softmax warps, rotary copies) meets partial blocks and missing keys. Two requests of
+    each shape are checked against the oracle."""
+    rng = np.random.default_rng(2027)
+    for case in range(4):
+        B = int(rng.integers(1, 41))
+        k = int(rng.integers(1, 2601))
+        S = k + int(rng.integers(0, 400))
+        H = int(rng.choice([8, 40, 128]))
+        w = tracegen.Workload("attr", 17, B=B, L=1, C=4 * S, S=S, k=k, E=656, kv_kind=tracegen.KV_DSA656,
+                              T=3, keep_pct=60, zipf_s=1.1, seed=100 + case)
+        ctx, sel, out = resolved_context(w, w.T, B)
+        orc = Oracle(B, w.C, w.S, w.E)
+        host = ctx.host_kv()
+        for t in range(w.T):
+            o_out, _, _ = orc.resolve(host, ctx.host_stride, sel[t])
+        assert np.array_equal(o_out, out.cpu().numpy()), case
+        pad = rng.random(o_out.shape) < 0.05  # padding among the selections
+        o_out = np.where(pad, -1, o_out).astype(np.int32)
+        q = bf16_tensor(rng.standard_normal((B, H, 576)))
+        sm = 1.0 / math.sqrt(576)
+        o_gpu, lse_gpu = run_attend(ctx, q.cuda(), torch.from_numpy(o_out).cuda(), sm)
+        qb = q.view(torch.int16).numpy().view(np.uint16)
+        for b in sorted({0, B - 1}):
+            o_ref, lse_ref, absw = orc.attend(b, qb[b], o_out[b], sm)
+            compare(o_gpu[b], lse_gpu[b], o_ref, lse_ref, absw, f"case {case} (B={B} k={k} S={S} H={H}) request {b}")
+        ctx.close()
+
+
 def test_attend_full_size_dsa_sampled():
     """32 requests x k = 2048 x 128 heads (the DSA workload), three requests checked."""
     w = tracegen.WORKLOADS["dsa"]
